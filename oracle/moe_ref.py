@@ -1,0 +1,359 @@
+"""Plain fp64 restatement of the single-device MoE layer: route, permute (with a
+simulated expert-parallel send layout), SwiGLU experts, unpermute + gate +
+scatter-add.  TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+Conventions.
+  T tokens, d hidden, E routed experts, k experts per token, f expert width,
+  n_ep simulated expert-parallel ranks, T_loc = T / n_ep tokens per rank.
+  An *assignment* is one (token, slot) pair; its flat index is a = t*k + j, with
+  j the slot in rank order of the token's chosen experts.  A = T*k.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "router_logits", "sigmoid", "select_experts", "gate_weights",
+    "capacity_rows", "permute", "ep_layout", "swiglu_expert",
+    "expert_outputs", "combine", "moe_forward", "dense_mask_forward",
+    "imbalance_eta", "alltoall_bytes", "dispatch_combine_bytes_per_token",
+]
+
+F64 = np.float64
+F32 = np.float32
+
+
+# ----------------------------------------------------------------------------
+# Step 1: route  ([EP] "Expert parallelism", step 1 "Route")
+# ----------------------------------------------------------------------------
+
+def router_logits(x, W_r, logit_bias=None):
+    """Router logits l[t, e] = sum_i x[t, i] * W_r[i, e] (+ logit_bias[e]), fp64.
+
+    x holds bf16 values (exactly representable in fp64); W_r is fp32.  [EP]
+    step 1 computes "the router" on the local tokens; the router is a linear map
+    of the token's hidden vector."""
+    l = np.asarray(x, F64) @ np.asarray(W_r, F64)
+    if logit_bias is not None:
+        l = l + np.asarray(logit_bias, F64)[None, :]
+    return l
+
+
+def sigmoid(l):
+    """Affinity s = 1 / (1 + exp(-l)) (DeepSeek-V3 style sigmoid scores, [EP]
+    "What DeepSeek-V3 did about it", node-limited routing by affinities)."""
+    l = np.asarray(l, F64)
+    return 1.0 / (1.0 + np.exp(-l))
+
+
+def _rank_order(values32, mask_out=None):
+    """Per row, the column indices sorted by (value descending, index ascending).
+
+    The order is a total order on fp32 values: -0.0 equals +0.0 (so the lower
+    index wins), NaN ranks below -inf, equal values keep index order.  numpy's
+    stable lexsort on (-value) gives exactly that: negation is exact, sorting
+    treats -0.0 == +0.0, and NaN sorts after +inf.  Columns with mask_out=True
+    rank after every other column."""
+    v = np.asarray(values32, F32)
+    n = v.shape[-1]
+    cols = np.broadcast_to(np.arange(n), v.shape)
+    keys = [cols, -v]
+    if mask_out is not None:
+        keys.append(np.asarray(mask_out, np.int8))
+    return np.lexsort(keys, axis=-1)
+
+
+def select_experts(scores, k, bias=None, n_groups=1, topk_groups=1):
+    """Top-k expert choice per token, int64 [T, k] in rank order.
+
+    scores: fp32 [T, E] (logits for softmax routing, sigmoid affinities for
+    sigmoid routing).  bias: optional fp32 [E] selection bias, the auxiliary-
+    loss-free balancing bias of [EPM] "Load balancing", (b): chosen =
+    TopK(logits + bias); it is added with one fp32 addition and never enters the
+    gates.
+
+    Group-limited (node-limited) routing, [EP] "What DeepSeek-V3 did about it":
+    experts are split into n_groups contiguous groups; a group's score is the
+    sum of the token's two highest (biased) values in it, computed as one fp32
+    addition; the topk_groups best groups are kept ("node limits must be applied
+    before final top-k", [EPS] "Failure modes"), and the k experts are chosen
+    among the kept groups.  Ties break toward the lower expert (or group) index.
+    """
+    v = np.asarray(scores, F32)
+    T, E = v.shape
+    if bias is not None:
+        v = (v + np.asarray(bias, F32)[None, :]).astype(F32)
+    if n_groups > 1:
+        gs = E // n_groups
+        vg = v.reshape(T, n_groups, gs)
+        srt = np.sort(-vg, axis=-1)                     # NaN last, i.e. lowest value
+        top1 = (-srt[..., 0]).astype(F32)
+        top2 = (-srt[..., 1]).astype(F32)
+        gscore = (top1 + top2).astype(F32)              # one fp32 addition
+        gorder = _rank_order(gscore)[:, :topk_groups]   # kept groups
+        keep = np.zeros((T, n_groups), bool)
+        np.put_along_axis(keep, gorder, True, axis=1)
+        excluded = ~np.repeat(keep, gs, axis=1)
+        order = _rank_order(v, excluded)
+    else:
+        order = _rank_order(v)
+    return order[:, :k].astype(np.int64)
+
+
+def gate_weights(scores, idx, score_fn, norm_topk):
+    """Gate of each chosen expert, fp64 [T, k].
+
+    softmax: g = exp(l_e - m) / sum_{e' < E} exp(l_e' - m) over all E logits
+    (router probability, [EPM] "Load balancing" (a): P_i is the router
+    probability); sigmoid: g = s_e.  With norm_topk the k gates are divided by
+    their sum (DeepSeek-V3's normalised gates).  The selection bias never enters
+    the gates ([EPM] "(b) Auxiliary-loss-free")."""
+    s = np.asarray(scores, F32).astype(F64)
+    idx = np.asarray(idx)
+    if score_fn == "softmax":
+        m = s.max(axis=1, keepdims=True)
+        p = np.exp(s - m)
+        p = p / p.sum(axis=1, keepdims=True)
+        g = np.take_along_axis(p, idx, axis=1)
+    elif score_fn == "sigmoid":
+        g = np.take_along_axis(s, idx, axis=1)
+    else:
+        raise ValueError(score_fn)
+    if norm_topk:
+        g = g / g.sum(axis=1, keepdims=True)
+    return g
+
+
+# ----------------------------------------------------------------------------
+# Step 2: permute  ([EP] step 2 "Permute"; "Token permutation and grouped GEMMs")
+# ----------------------------------------------------------------------------
+
+def capacity_rows(capacity_factor, T, k, E):
+    """Rows per expert under a capacity factor: CF times the fair share T*k/E,
+    rounded up ([EP] "Load imbalance becomes idle time": capping every expert at
+    CF times its fair share)."""
+    return int(math.ceil(capacity_factor * T * k / E))
+
+
+def permute(idx, E, capacity=0):
+    """Stable grouping of the T*k assignments into per-expert segments.
+
+    [EP] "Token permutation and grouped GEMMs": order is the stable argsort of
+    the expert ids, X[order] puts the rows in expert order, and the inverse
+    permutation inv[order] = arange(n) puts them back.
+
+    Returns a dict with
+      counts  int64 [E]   assignments routed to each expert (before any drop)
+      offsets int64 [E+1] first row of each expert's segment; dropless: the
+                          exclusive prefix sum of counts; capacity: e*cap
+      order   int64 [R]   row -> assignment a (-1 for a padding row)
+      inv     int64 [A]   assignment -> row (-1 for a dropped assignment)
+      kept    int64 [E]   rows holding data in each segment
+    Capacity mode ([EP] "Token permutation...", pad to capacity and batch): each
+    expert keeps its first `capacity` assignments in increasing a (the stable
+    order, i.e. dropping overflow by token order) and its segment is padded to
+    exactly `capacity` rows; R = E*capacity.  Dropless: R = A."""
+    flat = np.asarray(idx).reshape(-1).astype(np.int64)
+    A = flat.size
+    if A and (flat.min() < 0 or flat.max() >= E):
+        raise ValueError("expert id out of range")
+    srt = np.argsort(flat, kind="stable")               # positions in expert order
+    counts = np.bincount(flat, minlength=E).astype(np.int64)
+    starts = np.zeros(E + 1, np.int64)
+    starts[1:] = np.cumsum(counts)                       # exclusive prefix (+ total)
+    rank = np.arange(A, dtype=np.int64) - starts[flat[srt]]   # rank within expert
+    inv = np.full(A, -1, np.int64)
+    if capacity:
+        R = E * capacity
+        order = np.full(R, -1, np.int64)
+        keep = rank < capacity
+        rows = flat[srt][keep] * capacity + rank[keep]
+        order[rows] = srt[keep]
+        inv[srt[keep]] = rows
+        offsets = np.arange(E + 1, dtype=np.int64) * capacity
+        kept = np.minimum(counts, capacity)
+    else:
+        order = srt.astype(np.int64)
+        inv[srt] = np.arange(A, dtype=np.int64)
+        offsets = starts
+        kept = counts.copy()
+    return {"counts": counts, "offsets": offsets, "order": order, "inv": inv,
+            "kept": kept}
+
+
+def ep_layout(idx, inv, E, n_ep, T):
+    """Simulated expert-parallel send layout ([EP] steps 2-4 and "A dispatch you
+    can check by hand").
+
+    Expert e lives on rank floor(e*n_ep/E); token t belongs to source rank
+    floor(t/T_loc).  Each source rank sorts its (kept) assignments by
+    destination rank, and inside a destination by expert and then by a (a
+    stable sort, so the receiver's "sort by local expert", step 5, reproduces
+    the global per-expert order).  Returns
+      C        int64 [n_ep, n_ep]  C[s, q] = rows rank s sends to rank q
+      send_off int64 [n_ep, n_ep]  start of q's block in s's send buffer
+      recv_off int64 [n_ep, n_ep]  recv_off[q, s]: start of s's block in q's
+                                   receive buffer
+      send_idx int64 [A]           s's buffer occupies [s*T_loc*k, (s+1)*T_loc*k);
+                                   entry p holds the assignment a sent from that
+                                   slot, -1 past the last kept row
+    Combine sends the same blocks back (the transpose of C, [EP] "A dispatch
+    you can check by hand")."""
+    idx = np.asarray(idx)
+    T_, k = idx.shape
+    assert T_ == T
+    flat = idx.reshape(-1).astype(np.int64)
+    inv = np.asarray(inv)
+    T_loc = T // n_ep
+    dest = flat * n_ep // E
+    C = np.zeros((n_ep, n_ep), np.int64)
+    send_idx = np.full(T * k, -1, np.int64)
+    for s in range(n_ep):
+        a = np.arange(s * T_loc * k, (s + 1) * T_loc * k, dtype=np.int64)
+        a = a[inv[a] >= 0]                               # kept assignments only
+        o = np.lexsort((a, flat[a], dest[a]))            # by (dest, expert, a)
+        send_idx[s * T_loc * k: s * T_loc * k + a.size] = a[o]
+        C[s] = np.bincount(dest[a], minlength=n_ep)
+    send_off = np.zeros_like(C)
+    send_off[:, 1:] = np.cumsum(C, axis=1)[:, :-1]
+    recv_off = np.zeros_like(C)
+    recv_off[:, 1:] = np.cumsum(C.T, axis=1)[:, :-1]
+    return {"C": C, "send_off": send_off, "recv_off": recv_off,
+            "send_idx": send_idx}
+
+
+# ----------------------------------------------------------------------------
+# Step 5: expert compute ([EP] step 5; "How many bytes move": SwiGLU expert)
+# ----------------------------------------------------------------------------
+
+def swiglu_expert(X, W1, W3, W2):
+    """SwiGLU expert on rows X (fp64): W2 (silu(W1 x) * (W3 x)), with
+    silu(u) = u / (1 + exp(-u)).  W1, W3: [f, d]; W2: [d, f] (out, in).  One
+    expert holds the three d-by-d_e matrices of [EP] "DeepSeek-V3's layout,
+    counted" and costs 6*d*d_e FLOPs per row ([EP] "A worked example")."""
+    X = np.asarray(X, F64)
+    u = X @ np.asarray(W1, F64).T
+    v = X @ np.asarray(W3, F64).T
+    h = (u / (1.0 + np.exp(-u))) * v
+    return h @ np.asarray(W2, F64).T
+
+
+def expert_outputs(x, perm, k, W1, W3, W2, rows=None):
+    """Expert output of every row of the expert-grouped buffer (step 5: each
+    expert runs on its contiguous segment).  Returns fp64 [R, d]; rows not in
+    `rows`, and padding rows, stay zero.  W1/W3/W2 are indexable per expert."""
+    order = perm["order"]
+    R = order.size
+    x = np.asarray(x)
+    out = np.zeros((R, x.shape[1]), F64)
+    sel = np.ones(R, bool) if rows is None else np.zeros(R, bool)
+    if rows is not None:
+        sel[np.asarray(rows)] = True
+    offsets, kept = perm["offsets"], perm["kept"]
+    for e in range(kept.size):
+        rr = np.arange(int(offsets[e]), int(offsets[e]) + int(kept[e]))
+        rr = rr[sel[rr]]
+        if rr.size:
+            out[rr] = swiglu_expert(x[order[rr] // k], W1[e], W3[e], W2[e])
+    return out
+
+
+def combine(out_rows, perm, k, gates, T, shared_out=None):
+    """Step 7 ([EP] "Unpermute and weight"): undo the sort and scatter-add each
+    row into its token with its gate: y[t] += g[a] * out[row(a)] for every kept
+    assignment; dropped assignments add nothing.  A shared expert's output is
+    added to every token ([EPM] "Fine-grained vs coarse experts": shared experts
+    always active).  fp64."""
+    order = perm["order"]
+    g = np.asarray(gates, F64).reshape(-1)
+    y = np.zeros((T, out_rows.shape[1]), F64)
+    rows = np.nonzero(order >= 0)[0]
+    a = order[rows]
+    np.add.at(y, a // k, g[a][:, None] * out_rows[rows])
+    if shared_out is not None:
+        y += shared_out
+    return y
+
+
+def moe_forward(x, scores, cfg, W1, W3, W2, bias=None, tokens=None):
+    """The whole single-device layer, steps 1-7 of [EP] "Expert parallelism"
+    with the exchange steps 3, 4 and 6 being identities on one device.
+
+    x: bf16 values [T, d]; scores: fp32 [T, E] fed to selection; W1/W3/W2
+    indexable by expert (index E = the shared expert when cfg.has_shared).
+    tokens: optional subset of token ids whose outputs are computed (the other
+    rows of y are left zero); routing and permutation always cover all T.
+    Returns (y fp64 [T, d], dict of intermediates)."""
+    T, E, k = cfg.T, cfg.E, cfg.k
+    idx = select_experts(scores, k, bias, cfg.n_groups, cfg.topk_groups)
+    gates = gate_weights(scores, idx, cfg.score_fn, cfg.norm_topk)
+    perm = permute(idx, E, cfg.capacity)
+    rows = None
+    if tokens is not None:
+        tok = np.zeros(T, bool)
+        tok[np.asarray(tokens)] = True
+        order = perm["order"]
+        rows = np.nonzero((order >= 0) & tok[np.maximum(order, 0) // k])[0]
+    out = expert_outputs(x, perm, k, W1, W3, W2, rows)
+    shared = None
+    if cfg.has_shared:
+        shared = np.zeros((T, np.asarray(x).shape[1]), F64)
+        tt = np.arange(T) if tokens is None else np.asarray(tokens)
+        shared[tt] = swiglu_expert(np.asarray(x)[tt], W1[E], W3[E], W2[E])
+    y = combine(out, perm, k, gates, T, shared)
+    return y, {"idx": idx, "gates": gates, "perm": perm}
+
+
+def dense_mask_forward(x, scores, cfg, W1, W3, W2, bias=None):
+    """Brute force: run every expert on every token and weight by a dense
+    [T, E] gate mask that is zero outside each token's chosen experts.  Same
+    layer as `moe_forward` with no permutation at all; pure loops, for tiny
+    sizes only."""
+    T, E = cfg.T, cfg.E
+    idx = select_experts(scores, cfg.k, bias, cfg.n_groups, cfg.topk_groups)
+    gates = gate_weights(scores, idx, cfg.score_fn, cfg.norm_topk)
+    mask = np.zeros((T, E), F64)
+    for t in range(T):
+        for j in range(cfg.k):
+            mask[t, idx[t, j]] = gates[t, j]
+    x = np.asarray(x, F64)
+    y = np.zeros_like(x)
+    for e in range(E):
+        out = swiglu_expert(x, W1[e], W3[e], W2[e])
+        y += mask[:, e:e + 1] * out
+    if cfg.has_shared:
+        y += swiglu_expert(x, W1[E], W3[E], W2[E])
+    return y
+
+
+# ----------------------------------------------------------------------------
+# Layout metrics ([EP] "How many bytes move", "Load imbalance becomes idle time")
+# ----------------------------------------------------------------------------
+
+def imbalance_eta(C):
+    """Fraction of the group's expert compute doing useful work: the mean GPU
+    load over the busiest GPU's load, loads being column sums of the dispatch
+    matrix ([EP] "Load imbalance becomes idle time": a GPU with 50 % more than
+    its share runs the group at two thirds of its speed)."""
+    loads = np.asarray(C, F64).sum(axis=0)
+    return float(loads.mean() / loads.max())
+
+
+def alltoall_bytes(C, d, s_disp, s_comb):
+    """Bytes leaving each source rank in one dispatch and one combine: only
+    off-diagonal rows cross the network ([EP] "How many bytes move").  Returns
+    (dispatch_bytes[s], combine_bytes[s]); combine moves C transposed."""
+    C = np.asarray(C, np.int64)
+    off = C - np.diag(np.diag(C))
+    disp = off.sum(axis=1) * d * s_disp
+    comb = off.sum(axis=0) * d * s_comb
+    return disp, comb
+
+
+def dispatch_combine_bytes_per_token(k, d, s_disp, s_comb):
+    """Every token ships k copies of its d-vector out and gets k results back:
+    k*d*(s_disp + s_comb) bytes ([EPM] "The all-to-all pattern": 2 x top_k x
+    hidden x bytes)."""
+    return k * d * (s_disp + s_comb)
