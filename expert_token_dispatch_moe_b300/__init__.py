@@ -1,0 +1,188 @@
+"""B300-native single-device MoE layer hot path.
+
+Python binding of libmoe.so (C ABI, declared in include/moe.h): argument
+marshalling only.  Every step of the layer runs in the library's CUDA kernels;
+torch supplies device memory and streams.  There is no CPU fallback: importing
+this package fails if libmoe.so is missing, and every call raises MoeError when
+the library reports an error (including "no sm_103 device").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -m expert_token_dispatch_moe_b300.build`"
+        " (there is no fallback implementation)")
+_lib = ctypes.CDLL(LIB_PATH)
+
+MOE_SOFTMAX, MOE_SIGMOID = 0, 1
+ERRORS = {
+    0: "MOE_OK", -1: "MOE_E_NULL", -2: "MOE_E_SHAPE", -3: "MOE_E_ALIGN", -4: "MOE_E_WORKSPACE",
+    -5: "MOE_E_CUDA", -6: "MOE_E_DEVICE", -7: "MOE_E_DEVICE_DATA", -8: "MOE_E_DEVICE_TIMEOUT",
+}
+EXPORTS = ("moe_validate_cfg", "moe_grouped_rows", "moe_workspace_bytes", "moe_workspace_init",
+           "moe_router_logits", "moe_route", "moe_permute", "moe_ep_layout", "moe_pack_w13",
+           "moe_grouped_ffn", "moe_combine", "moe_get_device_status", "moe_strerror",
+           "moe_last_launch_count")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = _lib.moe_strerror(code).decode()
+        super().__init__(f"{where}: {ERRORS.get(code, code)} ({msg})")
+
+
+class MoeCfg(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("T", "d", "E", "k", "f", "n_ep", "score_fn", "norm_topk", "n_groups",
+                 "topk_groups", "capacity", "has_shared")]
+
+    @classmethod
+    def from_layer(cls, lc) -> "MoeCfg":
+        """From any object with the layer-configuration attributes (T, d, E, k,
+        f, n_ep, score_fn as "softmax"/"sigmoid" or 0/1, norm_topk, n_groups,
+        topk_groups, capacity, has_shared)."""
+        sf = lc.score_fn
+        if isinstance(sf, str):
+            sf = {"softmax": MOE_SOFTMAX, "sigmoid": MOE_SIGMOID}[sf]
+        return cls(lc.T, lc.d, lc.E, lc.k, lc.f, lc.n_ep, sf, lc.norm_topk, lc.n_groups,
+                   lc.topk_groups, lc.capacity, lc.has_shared)
+
+    @property
+    def A(self):
+        return self.T * self.k
+
+    @property
+    def R(self):
+        return self.E * self.capacity if self.capacity else self.T * self.k
+
+
+_P = ctypes.c_void_p
+_CFG = ctypes.POINTER(MoeCfg)
+_SZ = ctypes.c_size_t
+_sig = {
+    "moe_validate_cfg": (ctypes.c_int, [_CFG]),
+    "moe_grouped_rows": (ctypes.c_int64, [_CFG]),
+    "moe_workspace_bytes": (_SZ, [_CFG]),
+    "moe_workspace_init": (ctypes.c_int, [_CFG, _P, _SZ, _P]),
+    "moe_router_logits": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
+    "moe_route": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
+    "moe_permute": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_ep_layout": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_pack_w13": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
+    "moe_grouped_ffn": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
+    "moe_get_device_status": (ctypes.c_int, [_P, _P]),
+    "moe_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "moe_last_launch_count": (ctypes.c_int, []),
+}
+for _name, (_res, _args) in _sig.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype, _fn.argtypes = _res, _args
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise MoeError(rc, where)
+
+
+def _ws(ws):
+    return _ptr(ws), (ws.numel() * ws.element_size() if isinstance(ws, torch.Tensor) else 0)
+
+
+# ----------------------------------------------------------------------------
+# One wrapper per C entry point, same names and argument order.
+# ----------------------------------------------------------------------------
+
+def moe_validate_cfg(cfg: MoeCfg) -> int:
+    return _lib.moe_validate_cfg(ctypes.byref(cfg))
+
+
+def moe_grouped_rows(cfg: MoeCfg) -> int:
+    return _lib.moe_grouped_rows(ctypes.byref(cfg))
+
+
+def moe_workspace_bytes(cfg: MoeCfg) -> int:
+    return _lib.moe_workspace_bytes(ctypes.byref(cfg))
+
+
+def moe_workspace_init(cfg, ws, stream=None):
+    p, n = _ws(ws)
+    _check(_lib.moe_workspace_init(ctypes.byref(cfg), p, n, _stream(stream)), "moe_workspace_init")
+
+
+def moe_router_logits(cfg, x, W_r, logit_bias, scores, stream=None):
+    _check(_lib.moe_router_logits(ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(logit_bias),
+                                  _ptr(scores), _stream(stream)), "moe_router_logits")
+
+
+def moe_route(cfg, scores, bias, topk_idx, topk_gate, stream=None):
+    _check(_lib.moe_route(ctypes.byref(cfg), _ptr(scores), _ptr(bias), _ptr(topk_idx),
+                          _ptr(topk_gate), _stream(stream)), "moe_route")
+
+
+def moe_permute(cfg, x, topk_idx, counts, offsets, order, inv, x_sorted, ws, stream=None):
+    p, n = _ws(ws)
+    _check(_lib.moe_permute(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(counts),
+                            _ptr(offsets), _ptr(order), _ptr(inv), _ptr(x_sorted), p, n,
+                            _stream(stream)), "moe_permute")
+
+
+def moe_ep_layout(cfg, topk_idx, offsets, inv, count_mat, send_off, recv_off, send_idx, x,
+                  send_buf, ws, stream=None):
+    p, n = _ws(ws)
+    _check(_lib.moe_ep_layout(ctypes.byref(cfg), _ptr(topk_idx), _ptr(offsets), _ptr(inv),
+                              _ptr(count_mat), _ptr(send_off), _ptr(recv_off), _ptr(send_idx),
+                              _ptr(x), _ptr(send_buf), p, n, _stream(stream)), "moe_ep_layout")
+
+
+def moe_pack_w13(cfg, W1, W3, W13, stream=None):
+    _check(_lib.moe_pack_w13(ctypes.byref(cfg), _ptr(W1), _ptr(W3), _ptr(W13), _stream(stream)),
+           "moe_pack_w13")
+
+
+def moe_grouped_ffn(cfg, x_sorted, x, counts, offsets, W13, W2, h, y_sorted, ws, stream=None):
+    p, n = _ws(ws)
+    _check(_lib.moe_grouped_ffn(ctypes.byref(cfg), _ptr(x_sorted), _ptr(x), _ptr(counts),
+                                _ptr(offsets), _ptr(W13), _ptr(W2), _ptr(h), _ptr(y_sorted), p, n,
+                                _stream(stream)), "moe_grouped_ffn")
+
+
+def moe_combine(cfg, y_sorted, inv, topk_gate, y, stream=None):
+    _check(_lib.moe_combine(ctypes.byref(cfg), _ptr(y_sorted), _ptr(inv), _ptr(topk_gate), _ptr(y),
+                            _stream(stream)), "moe_combine")
+
+
+def moe_get_device_status(ws, stream=None) -> int:
+    return _lib.moe_get_device_status(_ptr(ws), _stream(stream))
+
+
+def moe_last_launch_count() -> int:
+    return _lib.moe_last_launch_count()
+
+
+from .layer import MoELayer  # noqa: E402,F401

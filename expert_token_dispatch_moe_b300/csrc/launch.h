@@ -1,0 +1,37 @@
+// Internal launcher declarations of libmoe (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Launch accounting for moe_last_launch_count (per host thread).
+void reset_launches();
+void note_launches(int n);
+
+int launch_router_logits(const moe_cfg& c, const void* x, const float* W, const float* lbias,
+                         float* out, cudaStream_t st);
+int launch_route(const moe_cfg& c, const float* scores, const float* bias, int32_t* idx,
+                 float* gate, cudaStream_t st);
+int launch_permute(const moe_cfg& c, const void* x, const int32_t* idx, int32_t* counts,
+                   int32_t* offsets, int32_t* order, int32_t* inv, void* x_sorted, void* ws,
+                   cudaStream_t st);
+int launch_ep_layout(const moe_cfg& c, const int32_t* idx, const int32_t* offsets,
+                     const int32_t* inv, int32_t* C, int32_t* send_off, int32_t* recv_off,
+                     int32_t* send_idx, const void* x, void* send_buf, void* ws, cudaStream_t st);
+int launch_pack_w13(const moe_cfg& c, const void* W1, const void* W3, void* W13, cudaStream_t st);
+int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
+                       const int32_t* counts, const int32_t* offsets, const void* W13,
+                       const void* W2, void* h, void* y_sorted, void* ws, cudaStream_t st);
+int launch_combine(const moe_cfg& c, const void* y_sorted, const int32_t* inv, const float* gate,
+                   void* y, cudaStream_t st);
+
+// Row move shared by the permute and the send-buffer fill: for each token t
+// and slot j, copy x[t] to dst[rows[t*k + j]] when that row is >= 0.
+int launch_row_scatter(const void* x, int T, int d, int k, const int32_t* rows, void* dst,
+                       cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,98 @@
+"""MoELayer: the whole single-device hot path as one object.
+
+Holds the layer's weights (with W1/W3 packed once for the grouped FFN) and
+every intermediate buffer, allocated once through torch on the current CUDA
+device, and runs the C-ABI steps in order on one stream:
+
+    moe_router_logits -> moe_route -> moe_permute -> moe_ep_layout
+      -> moe_grouped_ffn -> moe_combine
+
+(the seven steps of an expert-parallel MoE layer forward, with the exchange
+steps replaced by the simulated send layout on one device).
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (MoeCfg, moe_combine, moe_ep_layout, moe_grouped_ffn, moe_grouped_rows,
+               moe_last_launch_count, moe_pack_w13, moe_permute, moe_route, moe_router_logits,
+               moe_workspace_bytes, moe_workspace_init)
+
+
+class MoELayer:
+    def __init__(self, cfg, W1, W3, W2, W_r=None, logit_bias=None, selection_bias=None,
+                 device=None, with_send_buf=True):
+        self.cfg = cfg if isinstance(cfg, MoeCfg) else MoeCfg.from_layer(cfg)
+        c = self.cfg
+        dev = torch.device(device or "cuda")
+        self.device = dev
+        i32, f32, bf16 = torch.int32, torch.float32, torch.bfloat16
+        n_exp = c.E + c.has_shared
+        for w, shape in ((W1, (n_exp, c.f, c.d)), (W3, (n_exp, c.f, c.d)), (W2, (n_exp, c.d, c.f))):
+            if tuple(w.shape) != shape or w.dtype != bf16 or w.device.type != "cuda":
+                raise ValueError(f"expert weight must be bf16 cuda {shape}, got {tuple(w.shape)}")
+        self.W_r = W_r
+        self.logit_bias = logit_bias
+        self.selection_bias = selection_bias
+        self.W2 = W2.contiguous()
+        self.W13 = torch.empty(n_exp, 2 * c.f, c.d, dtype=bf16, device=dev)
+        moe_pack_w13(c, W1.contiguous(), W3.contiguous(), self.W13)
+        rows = moe_grouped_rows(c)
+        self.scores = torch.empty(c.T, c.E, dtype=f32, device=dev)
+        self.topk_idx = torch.empty(c.T, c.k, dtype=i32, device=dev)
+        self.topk_gate = torch.empty(c.T, c.k, dtype=f32, device=dev)
+        self.counts = torch.empty(c.E, dtype=i32, device=dev)
+        self.offsets = torch.empty(c.E + 1, dtype=i32, device=dev)
+        self.order = torch.empty(c.R, dtype=i32, device=dev)
+        self.inv = torch.empty(c.A, dtype=i32, device=dev)
+        self.x_sorted = torch.empty(c.R, c.d, dtype=bf16, device=dev)
+        self.count_mat = torch.empty(c.n_ep, c.n_ep, dtype=i32, device=dev)
+        self.send_off = torch.empty(c.n_ep, c.n_ep, dtype=i32, device=dev)
+        self.recv_off = torch.empty(c.n_ep, c.n_ep, dtype=i32, device=dev)
+        self.send_idx = torch.empty(c.A, dtype=i32, device=dev)
+        self.send_buf = torch.empty(c.A, c.d, dtype=bf16, device=dev) if with_send_buf else None
+        self.h = torch.empty(rows, c.f, dtype=bf16, device=dev)
+        self.y_sorted = torch.empty(rows, c.d, dtype=bf16, device=dev)
+        self.y = torch.empty(c.T, c.d, dtype=bf16, device=dev)
+        self.ws = torch.zeros(moe_workspace_bytes(c), dtype=torch.uint8, device=dev)
+        moe_workspace_init(c, self.ws)
+        self.launches_per_forward = None
+
+    def forward(self, x, scores=None):
+        """Run the layer on device tokens x (bf16 [T, d]); returns self.y.
+
+        With `scores` (fp32 [T, E]) the router step is skipped and the given
+        scores are routed (used to check routing on exact inputs)."""
+        c = self.cfg
+        n = 0
+        if scores is None:
+            moe_router_logits(c, x, self.W_r, self.logit_bias, self.scores)
+            n += moe_last_launch_count()
+            scores = self.scores
+        moe_route(c, scores, self.selection_bias, self.topk_idx, self.topk_gate)
+        n += moe_last_launch_count()
+        moe_permute(c, x, self.topk_idx, self.counts, self.offsets, self.order, self.inv,
+                    self.x_sorted, self.ws)
+        n += moe_last_launch_count()
+        moe_ep_layout(c, self.topk_idx, self.offsets, self.inv, self.count_mat, self.send_off,
+                      self.recv_off, self.send_idx, x if self.send_buf is not None else None,
+                      self.send_buf, self.ws)
+        n += moe_last_launch_count()
+        moe_grouped_ffn(c, self.x_sorted, x if c.has_shared else None, self.counts, self.offsets,
+                        self.W13, self.W2, self.h, self.y_sorted, self.ws)
+        n += moe_last_launch_count()
+        moe_combine(c, self.y_sorted, self.inv, self.topk_gate, self.y)
+        n += moe_last_launch_count()
+        self.launches_per_forward = n
+        return self.y
+
+    __call__ = forward
+
+    def forward_host(self, x_host, y_host, x_dev=None):
+        """End-to-end call with host buffers: copies pinned host x to the
+        device, runs the layer, copies y back into pinned host y_host."""
+        x_dev = x_dev if x_dev is not None else torch.empty_like(x_host, device=self.device)
+        x_dev.copy_(x_host, non_blocking=True)
+        y = self.forward(x_dev)
+        y_host.copy_(y, non_blocking=True)
+        return y_host

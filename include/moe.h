@@ -1,0 +1,217 @@
+/*
+ * moe.h -- C ABI of the single-device MoE layer hot path for NVIDIA B300
+ * (sm_103a): route, permute (with a simulated expert-parallel send layout),
+ * grouped SwiGLU expert FFN, and unpermute + gate + combine.
+ *
+ * The calls follow the seven-step forward pass of an expert-parallel MoE
+ * layer described in "Expert parallelism" (zerotofrontier.app, MoE chapter,
+ * section "Expert parallelism", steps 1-7).  On one device the exchange steps
+ * (3 counts, 4 dispatch, 6 combine) move nothing; moe_ep_layout produces the
+ * buffers, counts and offsets those exchanges would take.
+ *
+ * Conventions shared by every call
+ *  - Symbols: T tokens, d hidden size, E routed experts, k experts per token,
+ *    f expert FFN width, n_ep simulated expert-parallel ranks, T_loc = T/n_ep.
+ *    An assignment is one (token t, slot j) pair, flat index a = t*k + j, with
+ *    j the rank of the expert in the token's top-k order; A = T*k.
+ *    R = rows of the expert-grouped buffer: A when dropless, E*capacity with a
+ *    capacity.  Rows R .. R+T-1 of the FFN buffers belong to the shared expert
+ *    when cfg->has_shared.
+ *  - Every pointer argument is a DEVICE pointer unless stated otherwise, and
+ *    must be 16-byte aligned.  Matrices are dense and row-major.  bf16 values
+ *    are passed as their 16-bit patterns (moe_bf16).
+ *  - Ownership: the caller allocates and frees every buffer, including the
+ *    workspace.  The library allocates no device memory and never frees any.
+ *  - Every call is asynchronous on the caller's stream (cudaStream_t passed as
+ *    void*, NULL = legacy default stream) and never synchronises the host,
+ *    except moe_get_device_status.
+ *  - Errors: 0 on success; a negative MOE_E_* code otherwise.  Argument
+ *    errors are detected on the host before anything is launched.  Invalid
+ *    data found on the device (an expert id outside [0, E)) does not trap:
+ *    the kernel records MOE_E_DEVICE_DATA in the workspace status word, treats
+ *    the assignment as dropped, and moe_get_device_status reports it.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16;  /* bf16 bit pattern */
+
+enum { MOE_SOFTMAX = 0, MOE_SIGMOID = 1 };
+
+enum {
+  MOE_OK = 0,
+  MOE_E_NULL = -1,           /* a required pointer is NULL */
+  MOE_E_SHAPE = -2,          /* sizes violate the limits stated at moe_validate_cfg */
+  MOE_E_ALIGN = -3,          /* a pointer is not 16-byte aligned */
+  MOE_E_WORKSPACE = -4,      /* workspace NULL or smaller than moe_workspace_bytes */
+  MOE_E_CUDA = -5,           /* a CUDA runtime/driver call or a launch failed */
+  MOE_E_DEVICE = -6,         /* no sm_103 device is current */
+  MOE_E_DEVICE_DATA = -7,    /* device found an expert id outside [0, E) */
+  MOE_E_DEVICE_TIMEOUT = -8  /* a device-side wait gave up (kernel returned early) */
+};
+
+/* Layer configuration (plain data, passed by host pointer). */
+typedef struct moe_cfg {
+  int32_t T, d, E, k, f;       /* tokens, hidden, routed experts, top-k, FFN width */
+  int32_t n_ep;                /* simulated expert-parallel ranks */
+  int32_t score_fn;            /* MOE_SOFTMAX: scores are logits, gates = softmax over
+                                  all E; MOE_SIGMOID: scores are affinities, gates = s */
+  int32_t norm_topk;           /* 1: the k gates are divided by their sum */
+  int32_t n_groups;            /* group-limited routing over contiguous expert groups; */
+  int32_t topk_groups;         /*   (1, 1) = plain top-k                               */
+  int32_t capacity;            /* 0 = dropless; else rows kept per expert (pad to it) */
+  int32_t has_shared;          /* 1: one always-on shared expert of width f           */
+} moe_cfg;
+
+/* Host-only check of a configuration.  Limits:
+ *   T >= 1; 1 <= k <= min(E, 32); 1 <= E <= 1024; d % 64 == 0, 64 <= d <= 65536;
+ *   f % 128 == 0 (moe_grouped_ffn only; f >= 128);
+ *   n_ep >= 1, E % n_ep == 0, T % n_ep == 0;
+ *   n_groups >= 1, E % n_groups == 0, n_groups <= 32, E/n_groups >= 2 when n_groups > 1,
+ *   1 <= topk_groups <= n_groups, topk_groups*(E/n_groups) >= k;
+ *   capacity >= 0; has_shared in {0, 1}; score_fn in {MOE_SOFTMAX, MOE_SIGMOID};
+ *   T*k and R+T each below 2^31.
+ * Returns MOE_OK or MOE_E_SHAPE / MOE_E_NULL. */
+int moe_validate_cfg(const moe_cfg* cfg);
+
+/* Rows of the expert-grouped buffers: R (+T with a shared expert).  Host only. */
+int64_t moe_grouped_rows(const moe_cfg* cfg);
+
+/* Bytes of workspace the calls below need for this configuration (0 on an
+ * invalid configuration).  Host only. */
+size_t moe_workspace_bytes(const moe_cfg* cfg);
+
+/* Zero the workspace's device status word.  Call once after allocating the
+ * workspace.  ws_bytes is the size of the caller's workspace allocation; every
+ * call taking a workspace returns MOE_E_WORKSPACE when ws is NULL or ws_bytes <
+ * moe_workspace_bytes(cfg). */
+int moe_workspace_init(const moe_cfg* cfg, void* ws, size_t ws_bytes, void* stream);
+
+/* Step 1, the router ("Expert parallelism", step 1 "Route": compute the
+ * router for the local tokens).
+ *   x          bf16 [T, d]
+ *   W_r        fp32 [d, E]
+ *   logit_bias fp32 [E] or NULL: added to every token's logits
+ *   scores     fp32 [T, E] out: logits l = x W_r (+ logit_bias), fp32
+ *              accumulation; with MOE_SIGMOID the affinity 1/(1+exp(-l)). */
+int moe_router_logits(const moe_cfg* cfg, const moe_bf16* x, const float* W_r,
+                      const float* logit_bias, float* scores, void* stream);
+
+/* Step 1, top-k choice and gates ("Expert parallelism", step 1; node-limited
+ * routing in "What DeepSeek-V3 did about it"; the selection bias of "05 -
+ * Expert Parallelism (MoE)", "Load balancing" (b): chosen = TopK(logits + bias)).
+ *   scores    fp32 [T, E]
+ *   bias      fp32 [E] or NULL: selection bias, one fp32 add, never in gates
+ *   topk_idx  int32 [T, k] out: experts in rank order.  Order: larger
+ *             (score + bias) first, equal values -> lower expert index, -0.0 ==
+ *             +0.0, NaN below -inf.  Group-limited: a group's score is the fp32
+ *             sum of its two highest values; the topk_groups best groups (same
+ *             order rule) are kept and the k experts chosen among them.
+ *   topk_gate fp32 [T, k] out: softmax over all E scores (MOE_SOFTMAX) or the
+ *             score itself (MOE_SIGMOID); divided by the k gates' sum when
+ *             norm_topk. */
+int moe_route(const moe_cfg* cfg, const float* scores, const float* bias,
+              int32_t* topk_idx, float* topk_gate, void* stream);
+
+/* Step 2, permute ("Expert parallelism", step 2; "Token permutation and
+ * grouped GEMMs": order = stable argsort of expert ids, inv[order] = arange).
+ *   x         bf16 [T, d]
+ *   topk_idx  int32 [T, k]
+ *   counts    int32 [E] out: assignments routed to each expert (before drops)
+ *   offsets   int32 [E+1] out: first row of each expert's segment (dropless:
+ *             exclusive prefix sum of counts, offsets[E] = A; capacity: e*cap)
+ *   order     int32 [R] out: row -> assignment a (-1 for a padding row)
+ *   inv       int32 [A] out: assignment -> row (-1 when dropped)
+ *   x_sorted  bf16 [R, d] out: x_sorted[inv[a]] = x[a / k]; padding rows zero
+ *   ws        workspace; keeps the per-(source rank, expert) histogram that
+ *             moe_ep_layout reads
+ * Capacity: expert e keeps its first `capacity` assignments in increasing a. */
+int moe_permute(const moe_cfg* cfg, const moe_bf16* x, const int32_t* topk_idx,
+                int32_t* counts, int32_t* offsets, int32_t* order, int32_t* inv,
+                moe_bf16* x_sorted, void* ws, size_t ws_bytes, void* stream);
+
+/* Steps 2-4 as a layout: per-destination send buffers, the s->q count matrix
+ * and offsets ("Expert parallelism", step 2 "sort by destination GPU and
+ * count", step 3, step 4; "A dispatch you can check by hand").  Expert e lives
+ * on rank floor(e*n_ep/E); token t belongs to rank floor(t/T_loc).  Inside a
+ * rank's buffer rows are ordered by (destination, expert, a).
+ *   topk_idx, offsets, inv: as written by moe_route / moe_permute
+ *   ws        the workspace the preceding moe_permute wrote (same stream)
+ *   count_mat int32 [n_ep, n_ep] out: C[s][q] kept rows rank s sends to rank q
+ *   send_off  int32 [n_ep, n_ep] out: start of q's block in s's buffer
+ *   recv_off  int32 [n_ep, n_ep] out: recv_off[q][s] = start of s's block in
+ *             q's receive buffer
+ *   send_idx  int32 [A] out: rank s's buffer is rows [s*T_loc*k, (s+1)*T_loc*k);
+ *             entry p = the assignment sent from slot p, -1 past the kept rows
+ *   x         bf16 [T, d] or NULL
+ *   send_buf  bf16 [A, d] or NULL: when both are given, send_buf[p] =
+ *             x[send_idx[p] / k], zero where send_idx[p] == -1; giving only one
+ *             of the two is MOE_E_NULL.  n_ep <= 1024. */
+int moe_ep_layout(const moe_cfg* cfg, const int32_t* topk_idx, const int32_t* offsets,
+                  const int32_t* inv, int32_t* count_mat, int32_t* send_off,
+                  int32_t* recv_off, int32_t* send_idx, const moe_bf16* x,
+                  moe_bf16* send_buf, void* ws, size_t ws_bytes, void* stream);
+
+/* One-time weight packing for moe_grouped_ffn (not part of a layer step).
+ *   W1, W3    bf16 [E + has_shared, f, d]  (out, in)
+ *   W13       bf16 [E + has_shared, 2f, d] out: for each block b of 128 rows,
+ *             rows [256b, 256b+128) = W1 rows [128b, 128b+128) and rows
+ *             [256b+128, 256b+256) = W3 rows [128b, 128b+128), so that a
+ *             256-column accumulator tile holds matching gate and up columns. */
+int moe_pack_w13(const moe_cfg* cfg, const moe_bf16* W1, const moe_bf16* W3,
+                 moe_bf16* W13, void* stream);
+
+/* Step 5, the experts as one grouped product ("Expert parallelism", step 5;
+ * "Token permutation and grouped GEMMs", grouped GEMM; SwiGLU expert with
+ * 6*d*f FLOPs per row, "A worked example at DeepSeek-V3's shape").
+ *   x_sorted  bf16 [R, d]         (moe_permute)
+ *   x         bf16 [T, d] or NULL (needed when has_shared)
+ *   counts, offsets               (moe_permute); expert e's rows are
+ *             [offsets[e], offsets[e] + min(counts[e], capacity or inf))
+ *   W13       bf16 [E + has_shared, 2f, d]  (moe_pack_w13)
+ *   W2        bf16 [E + has_shared, d, f]   (out, in)
+ *   h         bf16 [R + has_shared*T, f] out: silu(x W1^T) * (x W3^T), fp32
+ *             accumulation, rounded to bf16; shared expert rows at R + t
+ *   y_sorted  bf16 [R + has_shared*T, d] out: h W2^T, fp32 accumulation
+ * Rows outside the experts' kept rows are not written.  E + has_shared <= 1025.
+ * The kernels are persistent (one CTA per SM); a device-side wait that exceeds
+ * one second records MOE_E_DEVICE_TIMEOUT in the workspace status word and the
+ * kernel returns early (outputs then incomplete). */
+int moe_grouped_ffn(const moe_cfg* cfg, const moe_bf16* x_sorted, const moe_bf16* x,
+                    const int32_t* counts, const int32_t* offsets,
+                    const moe_bf16* W13, const moe_bf16* W2, moe_bf16* h,
+                    moe_bf16* y_sorted, void* ws, size_t ws_bytes, void* stream);
+
+/* Step 7, unpermute and weight ("Expert parallelism", step 7: undo the sort
+ * and scatter-add each row into its token with its gate).  Computed as a
+ * per-token gather in slot order j = 0..k-1 with fp32 accumulation (the same
+ * sum, deterministic):
+ *   y[t] = sum_{j: inv[t*k+j] >= 0} topk_gate[t*k+j] * y_sorted[inv[t*k+j]]
+ *          (+ y_sorted[R + t] when has_shared), rounded to bf16.
+ *   y_sorted bf16 [R + has_shared*T, d]; inv int32 [A]; topk_gate fp32 [T, k]
+ *   y        bf16 [T, d] out */
+int moe_combine(const moe_cfg* cfg, const moe_bf16* y_sorted, const int32_t* inv,
+                const float* topk_gate, moe_bf16* y, void* stream);
+
+/* Synchronises `stream`, then returns and clears the workspace status word:
+ * MOE_OK, MOE_E_DEVICE_DATA or MOE_E_DEVICE_TIMEOUT (or MOE_E_CUDA). */
+int moe_get_device_status(void* ws, void* stream);
+
+/* Static description of an error code. */
+const char* moe_strerror(int code);
+
+/* Number of kernels the most recent successful call on this host thread
+ * launched (for launch accounting).  Host only. */
+int moe_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_B300_H */

@@ -1,0 +1,98 @@
+"""Host-side checks of the C ABI: the library loads, exports every entry point
+include/moe.h declares, and rejects bad arguments on the host before touching
+the device.  No kernel is launched (CPU only)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def m():
+    from expert_token_dispatch_moe_b300 import build
+    build.build()
+    import expert_token_dispatch_moe_b300 as mod
+    return mod
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    return set(re.findall(r"^\s*(?:const\s+)?[a-z0-9_]+\**\s+\**(moe_[a-z0-9_]+)\(", src, re.M))
+
+
+def test_header_declares_what_library_exports(m):
+    declared = _declared()
+    assert declared == set(m.EXPORTS)
+    out = subprocess.run(["nm", "-D", "--defined-only", m.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert exported == declared
+
+
+def test_validate_cfg_limits(m):
+    ok = m.MoeCfg.from_layer(synth.CONFIGS["dsv3"])
+    assert m.moe_validate_cfg(ok) == 0
+    for name in synth.CONFIGS:
+        assert m.moe_validate_cfg(m.MoeCfg.from_layer(synth.CONFIGS[name])) == 0
+    bad = [dict(k=0), dict(k=33), dict(E=1025), dict(d=100), dict(n_ep=3), dict(n_groups=7),
+           dict(topk_groups=9), dict(topk_groups=0), dict(capacity=-1), dict(has_shared=2),
+           dict(score_fn=5), dict(T=0), dict(n_groups=64, topk_groups=1)]
+    for b in bad:
+        c = m.MoeCfg.from_layer(synth.CONFIGS["dsv3"].with_(**b))
+        assert m.moe_validate_cfg(c) == -2, b
+    # too few experts in the kept groups for top-k
+    c = m.MoeCfg.from_layer(synth.CONFIGS["dsv3"].with_(topk_groups=1, k=33))
+    assert m.moe_validate_cfg(c) == -2
+    c = m.MoeCfg.from_layer(synth.CONFIGS["tiny"].with_(n_groups=4, topk_groups=1, k=3))
+    assert m.moe_validate_cfg(c) == -2
+    assert m._lib.moe_validate_cfg(None) == -1
+
+
+def test_workspace_and_rows(m):
+    c = m.MoeCfg.from_layer(synth.CONFIGS["skew"])
+    assert m.moe_grouped_rows(c) == 64 * 640
+    c = m.MoeCfg.from_layer(synth.CONFIGS["dsv3"])
+    assert m.moe_grouped_rows(c) == 8192 * 8 + 8192
+    assert m.moe_workspace_bytes(c) >= 256 + 4 * 8192 * 8
+    bad = m.MoeCfg.from_layer(synth.CONFIGS["dsv3"].with_(k=0))
+    assert m.moe_workspace_bytes(bad) == 0
+    assert m.moe_grouped_rows(bad) == -1
+
+
+def test_host_argument_errors(m):
+    """Null, misaligned and undersized arguments fail on the host; a valid
+    call on a machine without an sm_103 GPU fails with MOE_E_DEVICE."""
+    lib = m._lib
+    c = m.MoeCfg.from_layer(synth.CONFIGS["tiny"])
+    P = 1 << 20          # an aligned fake address: never dereferenced on the host
+    cfg = ctypes.byref(c)
+    assert lib.moe_route(cfg, None, None, P, P, None) == -1
+    assert lib.moe_route(cfg, P + 4, None, P, P, None) == -3
+    assert lib.moe_route(cfg, P, P + 8, P, P, None) == -3
+    ws_need = m.moe_workspace_bytes(c)
+    assert lib.moe_permute(cfg, P, P, P, P, P, P, P, None, ws_need, None) == -4
+    assert lib.moe_permute(cfg, P, P, P, P, P, P, P, P, ws_need - 1, None) == -4
+    assert lib.moe_ep_layout(cfg, P, P, P, P, P, P, P, P, None, P, ws_need, None) == -1
+    assert lib.moe_grouped_ffn(cfg, P, None, P, P, P, P, P, P, P, ws_need, None) in (-6,)
+    shared = m.MoeCfg.from_layer(synth.CONFIGS["tiny"].with_(has_shared=1))
+    assert lib.moe_grouped_ffn(ctypes.byref(shared), P, None, P, P, P, P, P, P, P,
+                               m.moe_workspace_bytes(shared), None) == -1
+    odd_f = m.MoeCfg.from_layer(synth.CONFIGS["tiny"].with_(f=200))
+    assert lib.moe_grouped_ffn(ctypes.byref(odd_f), P, None, P, P, P, P, P, P, P, ws_need,
+                               None) == -2
+    assert lib.moe_pack_w13(ctypes.byref(odd_f), P, P, P, None) == -2
+    bad = m.MoeCfg.from_layer(synth.CONFIGS["tiny"].with_(E=7))
+    assert lib.moe_route(ctypes.byref(bad), P, None, P, P, None) == -2
+    import torch
+    if not torch.cuda.is_available():
+        assert lib.moe_route(cfg, P, None, P, P, None) == -6
+        assert lib.moe_combine(cfg, P, P, P, P, None) == -6
+    assert lib.moe_get_device_status(None, None) == -4
+    for code in range(-8, 1):
+        assert lib.moe_strerror(code)
