@@ -1,0 +1,412 @@
+"""Benchmark of the single-device MoE layer hot path on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+One step = one pass of the whole hot path over one batch of synthetic tokens:
+router logits -> top-k route -> permute (expert-grouped buffer) -> simulated
+expert-parallel layout (count matrix, offsets, packed send buffer) -> grouped
+SwiGLU FFN (two tcgen05 grouped GEMMs) -> unpermute + gate + combine.
+
+Prints ONE JSON line (rank 0).  Default workload: the Mixtral-8x7B-shaped layer
+(T=4096, d=4096, E=8, f=14336, top-2, n_ep=8).  Inputs and weights are seeded
+random draws resident in HBM before timing; L2 is flushed (a 512 MiB write)
+between timed steps, outside the timed events.  With N > 1 (torchrun) every
+rank runs an independent replica of the layer on its own batch (weak scaling,
+no collective on the data path); the barrier and the max over ranks are for
+timing only.
+
+--impl reference times the oracle (fp64 numpy on the host cores) on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s on 1 B300; grouped-FFN % BF16 peak; permute/combine % HBM"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+def _workload(cfg):
+    s = (f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E} f={cfg.f} top-{cfg.k} {cfg.score_fn}"
+         f" n_ep={cfg.n_ep}")
+    if cfg.n_groups > 1:
+        s += f" groups={cfg.n_groups}/top{cfg.topk_groups}"
+    if cfg.has_shared:
+        s += " +1 shared"
+    if cfg.capacity:
+        s += f" capacity={cfg.capacity}"
+    return s
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class _Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}",
+                                          f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for ln in open(self.path):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[4:]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        mx = max(r[1] for r in rows)
+        load = [r for r in rows if r[0] > 0.3 * mx] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in load for i, v in enumerate(r[2][1:5])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": mx,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _algorithmic(cfg, counts_np):
+    """Algorithmic FLOPs and bytes of one step (what the method must do)."""
+    kept = int(np.minimum(counts_np, cfg.capacity).sum()) if cfg.capacity else cfg.A
+    rows_ffn = kept + (cfg.T if cfg.has_shared else 0)
+    R = cfg.R
+    b2 = 2  # bf16
+    out = {
+        "ffn_flops": 6.0 * cfg.d * cfg.f * rows_ffn,
+        "router_bytes": cfg.T * cfg.d * b2 + cfg.d * cfg.E * 4 + cfg.T * cfg.E * 4,
+        "route_bytes": cfg.T * cfg.E * 4 + cfg.A * 8,
+        "permute_bytes": cfg.T * cfg.d * b2 + R * cfg.d * b2 + 4 * (2 * cfg.A + R + 2 * cfg.E),
+        "layout_bytes": cfg.T * cfg.d * b2 + cfg.A * cfg.d * b2 + 4 * 4 * cfg.A,
+        "combine_bytes": (kept + (cfg.T if cfg.has_shared else 0)) * cfg.d * b2
+                         + cfg.T * cfg.d * b2 + 8 * cfg.A,
+        "rows_ffn": rows_ffn,
+    }
+    return out
+
+
+def run_ours(args, cfg):
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    import expert_token_dispatch_moe_b300 as m
+
+    x = synth.make_x(cfg, device=dev, seed=synth.DATA_SEED + rank)
+    W_r, lbias = synth.make_router(cfg, device=dev)
+    W1, W3, W2 = synth.make_expert_weights(cfg, device=dev)
+    layer = m.MoELayer(cfg, W1, W3, W2, W_r=W_r, logit_bias=lbias, device=dev)
+    del W1, W3
+    torch.cuda.empty_cache()
+    c = layer.cfg
+    st = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    names = ["router", "route", "permute", "ep_layout", "grouped_ffn", "combine"]
+
+    def step(ev):
+        ev[0].record(st)
+        m.moe_router_logits(c, x, layer.W_r, layer.logit_bias, layer.scores)
+        ev[1].record(st)
+        m.moe_route(c, layer.scores, None, layer.topk_idx, layer.topk_gate)
+        ev[2].record(st)
+        m.moe_permute(c, x, layer.topk_idx, layer.counts, layer.offsets, layer.order, layer.inv,
+                      layer.x_sorted, layer.ws)
+        ev[3].record(st)
+        m.moe_ep_layout(c, layer.topk_idx, layer.offsets, layer.inv, layer.count_mat,
+                        layer.send_off, layer.recv_off, layer.send_idx, x, layer.send_buf, layer.ws)
+        ev[4].record(st)
+        m.moe_grouped_ffn(c, layer.x_sorted, x if c.has_shared else None, layer.counts,
+                          layer.offsets, layer.W13, layer.W2, layer.h, layer.y_sorted, layer.ws)
+        ev[5].record(st)
+        m.moe_combine(c, layer.y_sorted, layer.inv, layer.topk_gate, layer.y)
+        ev[6].record(st)
+
+    # launches per step, from the library's own accounting
+    layer.forward(x)
+    launches_per_step = layer.launches_per_forward
+    for _ in range(args.warmup):
+        flush.zero_()
+        step([torch.cuda.Event(enable_timing=True) for _ in range(7)])
+    torch.cuda.synchronize(dev)
+    status = m.moe_get_device_status(layer.ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    clocks = _Clocks(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(6)]
+                    for i in range(args.steps)])  # ms
+    step_ms = float(per.sum(1).mean())
+    if world > 1:
+        t = torch.tensor([step_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t.item())
+    status = m.moe_get_device_status(layer.ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed steps")
+
+    # end to end through the public API, host buffers (pinned) in and out
+    x_host = x.cpu().pin_memory()
+    y_host = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(x)
+    e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(args.steps)]
+    for _ in range(2):
+        layer.forward_host(x_host, y_host, x_dev)
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        flush.zero_()
+        e_evs[i][0].record(st)
+        layer.forward_host(x_host, y_host, x_dev)
+        e_evs[i][1].record(st)
+    torch.cuda.synchronize(dev)
+    e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in e_evs]))
+
+    counts = layer.counts.cpu().numpy()
+    alg = _algorithmic(cfg, counts)
+    pk = _peaks()
+    kt = {n: float(per[:, j].mean()) for j, n in enumerate(names)}  # ms per call
+    ffn_tflops = alg["ffn_flops"] / (kt["grouped_ffn"] * 1e-3) / 1e12
+    gbs = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
+    kernels = {
+        "grouped_ffn": {"ms": kt["grouped_ffn"], "tflops": ffn_tflops,
+                        "frac_bf16_peak": ffn_tflops / pk["bf16_tflops"],
+                        "frac_bf16_sustained": (ffn_tflops / pk["bf16_tflops_sustained"]
+                                                if pk["bf16_tflops_sustained"] else None)},
+        "router": {"ms": kt["router"], "gbs": gbs(alg["router_bytes"], kt["router"])},
+        "route": {"ms": kt["route"], "gbs": gbs(alg["route_bytes"], kt["route"])},
+        "permute": {"ms": kt["permute"], "gbs": gbs(alg["permute_bytes"], kt["permute"]),
+                    "frac_hbm": gbs(alg["permute_bytes"], kt["permute"]) / pk["hbm_gbs"]},
+        "ep_layout": {"ms": kt["ep_layout"], "gbs": gbs(alg["layout_bytes"], kt["ep_layout"]),
+                      "frac_hbm": gbs(alg["layout_bytes"], kt["ep_layout"]) / pk["hbm_gbs"]},
+        "combine": {"ms": kt["combine"], "gbs": gbs(alg["combine_bytes"], kt["combine"]),
+                    "frac_hbm": gbs(alg["combine_bytes"], kt["combine"]) / pk["hbm_gbs"]},
+    }
+    res = {
+        "metric": METRIC,
+        "value": cfg.T * world / (step_ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded: x~N(0,1), expert weights~N(0,1/d), W_r~N(0,1/d) fp32)",
+        "config": {"workload": _workload(cfg), "tokens_per_gpu": cfg.T,
+                   "l2": "flushed between timed steps (512 MiB write, outside the timed events)",
+                   "parallelism": f"{world} independent replica(s)"},
+        "e2e": {"value": cfg.T * world / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 2},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": {"bound": "tensor", "kernel": "grouped_gemm_kernel (both GEMMs of one step)",
+                     "achieved": ffn_tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": ffn_tflops / pk["bf16_tflops"], "peak_source": pk["source"] + " burst",
+                     "traffic": None},
+        "kernels": kernels,
+        "wall_s": wall,
+    }
+    if clk:
+        res["clocks"] = clk
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(cfg, x, W_r, lbias, layer, budget_s=args.cpu_budget)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+def _cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def _oracle_sample(cfg, x_cpu, W_r_cpu, lbias_cpu, experts, n_tokens):
+    """The oracle on the first n_tokens tokens as a complete batch (router,
+    routing, permutation, EP layout, experts, combine).  Returns seconds."""
+    import oracle
+    sub = cfg.with_(T=n_tokens, n_ep=1)
+    xs = x_cpu[:n_tokens]
+    t0 = time.perf_counter()
+    l = oracle.router_logits(xs, W_r_cpu, lbias_cpu)
+    s = (oracle.sigmoid(l) if cfg.score_fn == "sigmoid" else l).astype(np.float32)
+    y, st = oracle.moe_forward(xs, s, sub, *experts)
+    oracle.ep_layout(st["idx"], st["perm"]["inv"], sub.E, 1, sub.T)
+    return time.perf_counter() - t0
+
+
+class _HostExperts:
+    def __init__(self, W):
+        self.W, self.c = W, {}
+
+    def __getitem__(self, e):
+        if e not in self.c:
+            self.c[e] = self.W[e].float().cpu().numpy()
+        return self.c[e]
+
+
+def cpu_baseline(cfg, x, W_r, lbias, layer=None, budget_s=15.0, W=None):
+    """Time the oracle, as it stands, on a bounded sample of the workload."""
+    x_cpu = x.float().cpu().numpy()
+    W_r_cpu = W_r.cpu().numpy()
+    lb = None if lbias is None else lbias.cpu().numpy()
+    if W is None:
+        W1 = torch.empty(0)
+        W13 = layer.W13  # packed [n, 2f, d]; unpack the 128-row interleave for the oracle
+        n, f2, d = W13.shape
+        f = f2 // 2
+        blk = W13.view(n, f // 128, 2, 128, d)
+        W1 = blk[:, :, 0].reshape(n, f, d)
+        W3 = blk[:, :, 1].reshape(n, f, d)
+        W = (W1, W3, layer.W2)
+    experts = tuple(_HostExperts(w) for w in W)
+    n2 = 8
+    _oracle_sample(cfg, x_cpu, W_r_cpu, lb, experts, n2)  # warms the host copy of the experts
+    t2 = _oracle_sample(cfg, x_cpu, W_r_cpu, lb, experts, n2)
+    # grow the sample until it takes about budget_s seconds (cost is not linear in
+    # the token count for small samples: per-expert weight conversion dominates)
+    while t2 < 0.5 * budget_s and n2 < cfg.T:
+        n2 = int(min(cfg.T, max(2 * n2, n2 * 0.8 * budget_s / max(t2, 1e-6))))
+        t2 = _oracle_sample(cfg, x_cpu, W_r_cpu, lb, experts, n2)
+    return {"value": n2 / t2, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+            "sample": f"first {n2} tokens of the workload as one batch (router, routing, "
+                      f"permutation, EP layout, SwiGLU experts, combine), fp64 numpy; {t2:.1f} s"}
+
+
+def run_reference(args, cfg):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    x = synth.make_x(cfg)
+    W_r, lbias = synth.make_router(cfg)
+    # weights of every expert (bf16 on the host); the oracle upcasts per expert
+    W1, W3, W2 = synth.make_expert_weights(cfg)
+    experts = tuple(_HostExperts(w) for w in (W1, W3, W2))
+    x_cpu = x.float().numpy()
+    W_r_cpu = W_r.numpy()
+    lb = None if lbias is None else lbias.numpy()
+    budget = max(3.0, min(args.cpu_budget, 150.0 / max(1, args.steps + args.warmup)))
+    n2 = 8
+    _oracle_sample(cfg, x_cpu, W_r_cpu, lb, experts, n2)
+    t = _oracle_sample(cfg, x_cpu, W_r_cpu, lb, experts, n2)
+    while t < 0.5 * budget and n2 < cfg.T:
+        n2 = int(min(cfg.T, max(2 * n2, n2 * 0.8 * budget / max(t, 1e-6))))
+        t = _oracle_sample(cfg, x_cpu, W_r_cpu, lb, experts, n2)
+    for _ in range(max(0, args.warmup - 2)):
+        _oracle_sample(cfg, x_cpu, W_r_cpu, lb, experts, n2)
+    times = [_oracle_sample(cfg, x_cpu, W_r_cpu, lb, experts, n2) for _ in range(args.steps)]
+    sec = float(np.mean(times))
+    v = n2 / sec
+    res = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3 * cfg.T / n2,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": _workload(cfg), "tokens_per_gpu": cfg.T,
+                   "parallelism": "host cores (oracle)"},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+                         "sample": f"first {n2} tokens per step as one batch, fp64 numpy"},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="mixtral", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    cfg = synth.CONFIGS[args.config]
+    if args.impl == "reference":
+        run_reference(args, cfg)
+    else:
+        run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

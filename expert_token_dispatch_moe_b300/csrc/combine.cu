@@ -63,13 +63,17 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
       y[size_t(t) * vec + v] = o;
     }
   } else {
-    for (int v = lane; v < vec; v += 32) {
+    // warp-uniform trip count: every lane takes part in the broadcasts
+    for (int v0 = 0; v0 < vec; v0 += 32) {
+      const int v = v0 + lane;
+      const bool active = v < vec;
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       for (int j = 0; j < k; ++j) {
         const int row = __shfl_sync(0xffffffffu, my_row, j);
         const float g = __shfl_sync(0xffffffffu, my_g, j);
-        if (row >= 0) fma_bf16x8(acc, __ldg(y_sorted + size_t(row) * vec + v), g);
+        if (row >= 0 && active) fma_bf16x8(acc, __ldg(y_sorted + size_t(row) * vec + v), g);
       }
+      if (!active) continue;
       if (has_shared) fma_bf16x8(acc, __ldg(shared_row + v), 1.0f);
       uint4 o;
       o.x = pack_bf16x2(acc[0], acc[1]);

@@ -166,11 +166,12 @@ __global__ void __launch_bounds__(256) row_scatter_kernel(const uint4* __restric
   if (t >= T) return;
   const int my_row = (lane < k) ? __ldg(rows + size_t(t) * k + lane) : -1;
   const uint4* src = x + size_t(t) * vec_per_row;
-  for (int v0 = lane; v0 < vec_per_row; v0 += 32 * 4) {
+  // warp-uniform trip count: every lane takes part in the row broadcasts
+  for (int v0 = 0; v0 < vec_per_row; v0 += 32 * 4) {
     uint4 buf[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int v = v0 + u * 32;
+      const int v = v0 + u * 32 + lane;
       if (v < vec_per_row) buf[u] = __ldg(src + v);
     }
     for (int j = 0; j < k; ++j) {
@@ -179,7 +180,7 @@ __global__ void __launch_bounds__(256) row_scatter_kernel(const uint4* __restric
       uint4* d = dst + size_t(row) * vec_per_row;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int v = v0 + u * 32;
+        const int v = v0 + u * 32 + lane;
         if (v < vec_per_row) d[v] = buf[u];
       }
     }
