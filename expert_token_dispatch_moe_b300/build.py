@@ -1,6 +1,6 @@
 """Build libmoe.so (the C-ABI CUDA library) in-tree for sm_103a with nvcc.
 
-    python -m expert_token_dispatch_moe_b300.build [--force] [-v]
+    python expert_token_dispatch_moe_b300/build.py [--force] [-v]
 
 The library links the CUDA runtime statically and reaches the driver API only
 through cudaGetDriverEntryPointByVersion, so it loads on a machine without a

@@ -15,8 +15,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def m():
-    from expert_token_dispatch_moe_b300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import expert_token_dispatch_moe_b300 as mod
     return mod
 
