@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
-        f"{LIB_PATH} is missing: build it with `python -m expert_token_dispatch_moe_b300.build`"
+        f"{LIB_PATH} is missing: build it with `python expert_token_dispatch_moe_b300/build.py`"
         " (there is no fallback implementation)")
 _lib = ctypes.CDLL(LIB_PATH)
 
@@ -26,9 +26,11 @@ MOE_SOFTMAX, MOE_SIGMOID = 0, 1
 ERRORS = {
     0: "MOE_OK", -1: "MOE_E_NULL", -2: "MOE_E_SHAPE", -3: "MOE_E_ALIGN", -4: "MOE_E_WORKSPACE",
     -5: "MOE_E_CUDA", -6: "MOE_E_DEVICE", -7: "MOE_E_DEVICE_DATA", -8: "MOE_E_DEVICE_TIMEOUT",
+    -9: "MOE_E_SCRATCH_LIMIT",
 }
 EXPORTS = ("moe_validate_cfg", "moe_grouped_rows", "moe_workspace_bytes", "moe_workspace_init",
-           "moe_router_logits", "moe_route", "moe_permute", "moe_ep_layout", "moe_pack_w13",
+           "moe_router_logits", "moe_route", "moe_permute", "moe_permute_noalloc",
+           "moe_ep_layout", "moe_pack_w13",
            "moe_grouped_ffn", "moe_combine", "moe_get_device_status", "moe_strerror",
            "moe_last_launch_count")
 
@@ -76,6 +78,7 @@ _sig = {
     "moe_router_logits": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
     "moe_route": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
     "moe_permute": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_permute_noalloc": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_ep_layout": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_pack_w13": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
     "moe_grouped_ffn": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -150,6 +153,14 @@ def moe_permute(cfg, x, topk_idx, counts, offsets, order, inv, x_sorted, ws, str
     _check(_lib.moe_permute(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(counts),
                             _ptr(offsets), _ptr(order), _ptr(inv), _ptr(x_sorted), p, n,
                             _stream(stream)), "moe_permute")
+
+
+def moe_permute_noalloc(cfg, x, topk_idx, counts, offsets, order, inv, x_sorted, stream=None):
+    """moe_permute for callers that cannot allocate: no workspace argument, the
+    library's fixed device scratch is used (calls must not overlap on the GPU)."""
+    _check(_lib.moe_permute_noalloc(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(counts),
+                                    _ptr(offsets), _ptr(order), _ptr(inv), _ptr(x_sorted),
+                                    _stream(stream)), "moe_permute_noalloc")
 
 
 def moe_ep_layout(cfg, topk_idx, offsets, inv, count_mat, send_off, recv_off, send_idx, x,

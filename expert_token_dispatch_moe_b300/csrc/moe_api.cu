@@ -223,6 +223,8 @@ MOE_API const char* moe_strerror(int code) {
     case MOE_E_DEVICE: return "the current device is not an sm_103 GPU";
     case MOE_E_DEVICE_DATA: return "an expert id outside [0, E) was found on the device";
     case MOE_E_DEVICE_TIMEOUT: return "a device-side wait timed out";
+    case MOE_E_SCRATCH_LIMIT:
+      return "moe_permute_noalloc: configuration needs more than its fixed 1 MiB device scratch";
     default: return "unknown error";
   }
 }

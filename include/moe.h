@@ -54,7 +54,9 @@ enum {
   MOE_E_CUDA = -5,           /* a CUDA runtime/driver call or a launch failed */
   MOE_E_DEVICE = -6,         /* no sm_103 device is current */
   MOE_E_DEVICE_DATA = -7,    /* device found an expert id outside [0, E) */
-  MOE_E_DEVICE_TIMEOUT = -8  /* a device-side wait gave up (kernel returned early) */
+  MOE_E_DEVICE_TIMEOUT = -8, /* a device-side wait gave up (kernel returned early) */
+  MOE_E_SCRATCH_LIMIT = -9   /* moe_permute_noalloc: the configuration needs more scratch
+                                than the library's fixed 1 MiB device array holds */
 };
 
 /* Layer configuration (plain data, passed by host pointer). */
@@ -158,6 +160,31 @@ int moe_ep_layout(const moe_cfg* cfg, const int32_t* topk_idx, const int32_t* of
                   const int32_t* inv, int32_t* count_mat, int32_t* send_off,
                   int32_t* recv_off, int32_t* send_idx, const moe_bf16* x,
                   moe_bf16* send_buf, void* ws, size_t ws_bytes, void* stream);
+
+/* moe_permute without a workspace argument, for callers that cannot allocate
+ * device memory.  The pages have no counterpart to this entry point; it exists
+ * for integration.  Some callers are handed only their input and output tensors
+ * (for example a plugin inside an inference runtime with no allocator hook), and
+ * some must not call cudaMalloc on a serving path, because it can synchronise
+ * the device.  Such callers cannot provide the workspace that moe_permute needs.
+ *
+ * Outputs, arguments and results are those of moe_permute.  The scratch lives in
+ * a fixed 1 MiB array in device memory that the library holds on every GPU that
+ * loads it, until the process exits.
+ *  - A configuration whose permute scratch (status word, per-(rank, expert)
+ *    counts and per-2048-assignment histograms) exceeds 1 MiB is rejected on the
+ *    host with MOE_E_SCRATCH_LIMIT.
+ *  - The first call on a device looks up the array's device address.  Make that
+ *    first call before any stream capture on that device.
+ *  - Every call shares the one array.  Calls that overlap on the GPU (on
+ *    different streams, or from host threads without ordering) race on it.
+ *  - Each call clears the status word and counters it uses.  Bad expert ids are
+ *    treated as dropped (inv = -1) as in moe_permute, but the status word is not
+ *    readable from outside.
+ *  - The call allocates and frees nothing. */
+int moe_permute_noalloc(const moe_cfg* cfg, const moe_bf16* x, const int32_t* topk_idx,
+                        int32_t* counts, int32_t* offsets, int32_t* order, int32_t* inv,
+                        moe_bf16* x_sorted, void* stream);
 
 /* One-time weight packing for moe_grouped_ffn (not part of a layer step).
  *   W1, W3    bf16 [E + has_shared, f, d]  (out, in)
