@@ -163,7 +163,8 @@ def run_ours(args, cfg):
 
     def step(ev):
         ev[0].record(st)
-        m.moe_router_logits(c, x, layer.W_r, layer.logit_bias, layer.scores)
+        m.moe_router_logits(c, x, layer.W_r, layer.W_r_split, layer.logit_bias, layer.scores,
+                            layer.ws)
         ev[1].record(st)
         m.moe_route(c, layer.scores, None, layer.topk_idx, layer.topk_gate)
         ev[2].record(st)

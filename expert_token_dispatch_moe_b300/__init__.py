@@ -29,7 +29,7 @@ ERRORS = {
     -9: "MOE_E_SCRATCH_LIMIT",
 }
 EXPORTS = ("moe_validate_cfg", "moe_grouped_rows", "moe_workspace_bytes", "moe_workspace_init",
-           "moe_router_logits", "moe_route", "moe_permute", "moe_permute_noalloc",
+           "moe_pack_router", "moe_router_logits", "moe_route", "moe_permute", "moe_permute_noalloc",
            "moe_ep_layout", "moe_pack_w13",
            "moe_grouped_ffn", "moe_combine", "moe_get_device_status", "moe_strerror",
            "moe_last_launch_count")
@@ -75,7 +75,8 @@ _sig = {
     "moe_grouped_rows": (ctypes.c_int64, [_CFG]),
     "moe_workspace_bytes": (_SZ, [_CFG]),
     "moe_workspace_init": (ctypes.c_int, [_CFG, _P, _SZ, _P]),
-    "moe_router_logits": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
+    "moe_pack_router": (ctypes.c_int, [_CFG, _P, _P, _P]),
+    "moe_router_logits": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_route": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
     "moe_permute": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute_noalloc": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P]),
@@ -138,9 +139,16 @@ def moe_workspace_init(cfg, ws, stream=None):
     _check(_lib.moe_workspace_init(ctypes.byref(cfg), p, n, _stream(stream)), "moe_workspace_init")
 
 
-def moe_router_logits(cfg, x, W_r, logit_bias, scores, stream=None):
-    _check(_lib.moe_router_logits(ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(logit_bias),
-                                  _ptr(scores), _stream(stream)), "moe_router_logits")
+def moe_pack_router(cfg, W_r, W_r_split, stream=None):
+    _check(_lib.moe_pack_router(ctypes.byref(cfg), _ptr(W_r), _ptr(W_r_split), _stream(stream)),
+           "moe_pack_router")
+
+
+def moe_router_logits(cfg, x, W_r, W_r_split, logit_bias, scores, ws=None, stream=None):
+    p, n = _ws(ws)
+    _check(_lib.moe_router_logits(ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(W_r_split),
+                                  _ptr(logit_bias), _ptr(scores), p, n, _stream(stream)),
+           "moe_router_logits")
 
 
 def moe_route(cfg, scores, bias, topk_idx, topk_gate, stream=None):

@@ -40,15 +40,25 @@ constexpr uint64_t DRAIN_NS = 100000000ull;
 constexpr size_t DYN_SMEM = size_t(STAGES) * STAGE_BYTES + 1024;
 }  // namespace gg
 
+enum { kEpiSwiglu = 0, kEpiBf16 = 1, kEpiF32 = 2 };
+
 struct GroupedParams {
-  const int32_t* counts;
+  const int32_t* counts;  // nullptr: one dense segment of dense_rows rows at row 0
   const int32_t* offsets;
   int E, capacity, has_shared, T, R;
-  int K;                  // reduction length
+  int dense_rows;
+  int K;                  // reduction length of one pass
+  int k_passes;           // passes over K: A re-read each pass, B advanced by b_pass_rows
+  int b_pass_rows;
   int N;                  // weight rows per expert (output columns before SwiGLU)
-  int swiglu;             // 1: out[:, j] = silu(acc[:, gate j]) * acc[:, up j]
+  int mode;               // kEpiSwiglu: out[:, j] = silu(acc[:, gate j]) * acc[:, up j]
+                          // kEpiBf16:   out = bf16(acc)
+                          // kEpiF32:    out_f32 = acc + col_bias (sigmoid if set), fp32
   int shared_a_separate;  // 1: shared expert's A rows come from tmA_sh from row 0
   __nv_bfloat16* out;
+  float* out_f32;
+  const float* col_bias;
+  int sigmoid;
   int ld_out;
   int* status;
 };
@@ -67,7 +77,11 @@ struct GroupedCtl {
 
 __device__ __forceinline__ void segment(const GroupedParams& p, int g, int& rows, int& a_row0,
                                         int& out_row0) {
-  if (g < p.E) {
+  if (p.counts == nullptr) {
+    rows = p.dense_rows;
+    a_row0 = 0;
+    out_row0 = 0;
+  } else if (g < p.E) {
     const int c = __ldg(p.counts + g);
     rows = p.capacity ? min(c, p.capacity) : c;
     a_row0 = __ldg(p.offsets + g);
@@ -106,9 +120,10 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) &
                                              ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_seg = p.E + p.has_shared;
+  const int n_seg = p.counts ? p.E + p.has_shared : 1;
   const int n_blocks_n = (p.N + BN - 1) / BN;
-  const int num_kb = p.K / BK;
+  const int kb_per_pass = p.K / BK;
+  const int num_kb = kb_per_pass * p.k_passes;
 
   // ---- device-side tile schedule: exclusive prefix of tiles per segment ----
   {
@@ -196,16 +211,19 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         int g, m_blk, n_blk, rows, a_row0, out_row0;
         decode(t, g, m_blk, n_blk, rows, a_row0, out_row0);
-        const CUtensorMap* ma = (g >= p.E && p.shared_a_separate) ? &tmA_sh : &tmA;
+        const CUtensorMap* ma =
+            (p.counts && g >= p.E && p.shared_a_separate) ? &tmA_sh : &tmA;
         const int a_row = a_row0 + m_blk * BM;
         const int b_row = g * p.N + n_blk * BN;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!wait_or_abort(&ctl.empty[stage], phase ^ 1u, ctl, p.status)) { ok = false; break; }
           uint8_t* sa = smem + stage * STAGE_BYTES;
           uint8_t* sb = sa + A_BYTES;
+          const int pass = kb / kb_per_pass;
+          const int ka = (kb - pass * kb_per_pass) * BK;
           mbar_arrive_expect_tx(&ctl.full[stage], STAGE_BYTES);
-          tma_load_2d(sa, ma, kb * BK, a_row, &ctl.full[stage]);
-          tma_load_2d(sb, &tmB, kb * BK, b_row, &ctl.full[stage]);
+          tma_load_2d(sa, ma, ka, a_row, &ctl.full[stage]);
+          tma_load_2d(sb, &tmB, ka, b_row + pass * p.b_pass_rows, &ctl.full[stage]);
           issued |= 1u << stage;
           last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -268,8 +286,30 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
       const uint32_t taddr = tmem_base + acc * BN + (uint32_t(quarter * 32) << 16);
       const int r = m_blk * BM + row_in_tile;
       const bool valid = r < rows;
-      __nv_bfloat16* orow = p.out + size_t(out_row0 + (valid ? r : 0)) * p.ld_out;
-      if (p.swiglu) {
+      const size_t orow_idx = size_t(out_row0 + (valid ? r : 0)) * p.ld_out;
+      __nv_bfloat16* orow = p.out + orow_idx;
+      if (p.mode == kEpiF32) {
+        const int col0 = n_blk * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(taddr + c, v);
+          tmem_ld_wait();
+          if (valid && col0 + c < p.N) {
+            float* dst = p.out_f32 + orow_idx + col0 + c;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int col = col0 + c + i;
+              if (col < p.N) {
+                float l = __uint_as_float(v[i]);
+                if (p.col_bias) l += __ldg(p.col_bias + col);
+                if (p.sigmoid) l = 1.0f / (1.0f + expf(-l));
+                dst[i] = l;
+              }
+            }
+          }
+        }
+      } else if (p.mode == kEpiSwiglu) {
         const int col0 = n_blk * (BN / 2);
 #pragma unroll 1
         for (int c = 0; c < BN / 2; c += 32) {
@@ -377,6 +417,16 @@ static bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t co
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+static int set_smem_attr() {
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               int(gg::DYN_SMEM));
+  });
+  return err == cudaSuccess ? MOE_OK : MOE_E_CUDA;
+}
+
 static int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -395,18 +445,74 @@ int launch_pack_w13(const moe_cfg& c, const void* W1, const void* W3, void* W13,
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_E_CUDA;
 }
 
+// Router logits on the tensor cores: x [T, d] (bf16) times the three bf16
+// terms of W_r (W_r = hi + mid + lo exactly, stored [3][E][d]), accumulated in
+// fp32 in tensor memory over 3 passes of K, + logit bias, sigmoid if asked.
+int launch_router_tc(const moe_cfg& c, const void* x, const void* W_split, const float* lbias,
+                     float* out, int* status, cudaStream_t st) {
+  using namespace gg;
+  if (!get_encoder()) return MOE_E_CUDA;
+  if (set_smem_attr() != MOE_OK) return MOE_E_CUDA;
+  CUtensorMap mA, mB;
+  if (!make_map(&mA, x, uint64_t(c.T), c.d, BM)) return MOE_E_CUDA;
+  if (!make_map(&mB, W_split, uint64_t(3) * c.E, c.d, BN)) return MOE_E_CUDA;
+  const int sms = sm_count();
+  if (sms <= 0) return MOE_E_CUDA;
+  GroupedParams p{};
+  p.counts = nullptr;
+  p.dense_rows = c.T;
+  p.K = c.d;
+  p.k_passes = 3;
+  p.b_pass_rows = c.E;
+  p.N = c.E;
+  p.mode = kEpiF32;
+  p.out_f32 = out;
+  p.col_bias = lbias;
+  p.sigmoid = c.score_fn == MOE_SIGMOID;
+  p.ld_out = c.E;
+  p.status = status;
+  const long long tiles = (long long)((c.T + BM - 1) / BM) * ((c.E + BN - 1) / BN);
+  const int grid = int(tiles < sms ? tiles : sms);
+  grouped_gemm_kernel<<<grid, THREADS, DYN_SMEM, st>>>(mA, mA, mB, p);
+  note_launches(1);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_E_CUDA;
+}
+
+// Exact three-term bf16 split of the fp32 router weights, transposed to
+// K-major: out[s][e][i] for W_r[i][e] = hi + mid + lo.
+__global__ void __launch_bounds__(256) pack_router_kernel(const float* __restrict__ W, int d, int E,
+                                                          __nv_bfloat16* __restrict__ out) {
+  const long long n = (long long)d * E;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int i = int(idx / E), e = int(idx % E);
+    const float w = W[idx];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+    const size_t o = size_t(e) * d + i;
+    out[o] = hi;
+    out[size_t(E) * d + o] = mid;
+    out[size_t(2) * E * d + o] = lo;
+  }
+}
+
+int launch_pack_router(const moe_cfg& c, const float* W, void* out, cudaStream_t st) {
+  const long long n = (long long)c.d * c.E;
+  const int blocks = int((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  pack_router_kernel<<<blocks, 256, 0, st>>>(W, c.d, c.E, static_cast<__nv_bfloat16*>(out));
+  note_launches(1);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_E_CUDA;
+}
+
 int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
                        const int32_t* counts, const int32_t* offsets, const void* W13,
                        const void* W2, void* h, void* y_sorted, void* ws, cudaStream_t st) {
   using namespace gg;
   if (!get_encoder()) return MOE_E_CUDA;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(DYN_SMEM)) != cudaSuccess)
-      return MOE_E_CUDA;
-    attr_done = true;
-  }
+  if (set_smem_attr() != MOE_OK) return MOE_E_CUDA;
   const WsLayout L = ws_layout(c);
   const int R = c.capacity ? c.E * c.capacity : c.T * c.k;
   const int n_exp = c.E + c.has_shared;
@@ -436,7 +542,8 @@ int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
   p1.R = R;
   p1.K = c.d;
   p1.N = 2 * c.f;
-  p1.swiglu = 1;
+  p1.k_passes = 1;
+  p1.mode = kEpiSwiglu;
   p1.shared_a_separate = 1;
   p1.out = static_cast<__nv_bfloat16*>(h);
   p1.ld_out = c.f;
@@ -448,7 +555,7 @@ int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
   GroupedParams p2 = p1;
   p2.K = c.f;
   p2.N = c.d;
-  p2.swiglu = 0;
+  p2.mode = kEpiBf16;
   p2.shared_a_separate = 0;
   p2.out = static_cast<__nv_bfloat16*>(y_sorted);
   p2.ld_out = c.d;

@@ -112,14 +112,31 @@ MOE_API int moe_workspace_init(const moe_cfg* c, void* ws, size_t ws_bytes, void
   return MOE_OK;
 }
 
-MOE_API int moe_router_logits(const moe_cfg* c, const moe_bf16* x, const float* W_r,
-                              const float* logit_bias, float* scores, void* stream) {
+MOE_API int moe_pack_router(const moe_cfg* c, const float* W_r, moe_bf16* W_r_split,
+                            void* stream) {
   reset_launches();
   MOE_TRY(moe_validate_cfg(c));
-  MOE_TRY(check_ptrs({x, W_r, scores}));
-  MOE_TRY(check_opt({logit_bias}));
+  MOE_TRY(check_ptrs({W_r, W_r_split}));
   MOE_TRY(device_ok());
-  return launch_router_logits(*c, x, W_r, logit_bias, scores, static_cast<cudaStream_t>(stream));
+  return launch_pack_router(*c, W_r, W_r_split, static_cast<cudaStream_t>(stream));
+}
+
+MOE_API int moe_router_logits(const moe_cfg* c, const moe_bf16* x, const float* W_r,
+                              const moe_bf16* W_r_split, const float* logit_bias, float* scores,
+                              void* ws, size_t ws_bytes, void* stream) {
+  reset_launches();
+  MOE_TRY(moe_validate_cfg(c));
+  MOE_TRY(check_ptrs({x, scores}));
+  MOE_TRY(check_opt({W_r, W_r_split, logit_bias}));
+  if (!W_r && !W_r_split) return MOE_E_NULL;
+  if (ws) MOE_TRY(check_ws(c, ws, ws_bytes));
+  MOE_TRY(device_ok());
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (W_r_split) {
+    int* status = ws ? ws_ptr<int>(ws, ws_layout(*c).status) : nullptr;
+    return launch_router_tc(*c, x, W_r_split, logit_bias, scores, status, st);
+  }
+  return launch_router_logits(*c, x, W_r, logit_bias, scores, st);
 }
 
 MOE_API int moe_route(const moe_cfg* c, const float* scores, const float* bias, int32_t* topk_idx,

@@ -15,13 +15,18 @@ from __future__ import annotations
 import torch
 
 from . import (MoeCfg, moe_combine, moe_ep_layout, moe_grouped_ffn, moe_grouped_rows,
-               moe_last_launch_count, moe_pack_w13, moe_permute, moe_route, moe_router_logits,
-               moe_workspace_bytes, moe_workspace_init)
+               moe_last_launch_count, moe_pack_router, moe_pack_w13, moe_permute, moe_route,
+               moe_router_logits, moe_workspace_bytes, moe_workspace_init)
+
+# Routers with at least this many experts run on the tensor cores (three-term
+# bf16 split of the fp32 weights); smaller ones are bandwidth-bound SIMT dot
+# products.
+TC_ROUTER_MIN_E = 17
 
 
 class MoELayer:
     def __init__(self, cfg, W1, W3, W2, W_r=None, logit_bias=None, selection_bias=None,
-                 device=None, with_send_buf=True):
+                 device=None, with_send_buf=True, tc_router=None):
         self.cfg = cfg if isinstance(cfg, MoeCfg) else MoeCfg.from_layer(cfg)
         c = self.cfg
         dev = torch.device(device or "cuda")
@@ -32,6 +37,12 @@ class MoELayer:
             if tuple(w.shape) != shape or w.dtype != bf16 or w.device.type != "cuda":
                 raise ValueError(f"expert weight must be bf16 cuda {shape}, got {tuple(w.shape)}")
         self.W_r = W_r
+        self.W_r_split = None
+        if tc_router is None:
+            tc_router = c.E >= TC_ROUTER_MIN_E
+        if W_r is not None and tc_router:
+            self.W_r_split = torch.empty(3, c.E, c.d, dtype=bf16, device=dev)
+            moe_pack_router(c, W_r, self.W_r_split)
         self.logit_bias = logit_bias
         self.selection_bias = selection_bias
         self.W2 = W2.contiguous()
@@ -66,7 +77,8 @@ class MoELayer:
         c = self.cfg
         n = 0
         if scores is None:
-            moe_router_logits(c, x, self.W_r, self.logit_bias, self.scores)
+            moe_router_logits(c, x, self.W_r, self.W_r_split, self.logit_bias, self.scores,
+                              self.ws)
             n += moe_last_launch_count()
             scores = self.scores
         moe_route(c, scores, self.selection_bias, self.topk_idx, self.topk_gate)

@@ -96,15 +96,28 @@ size_t moe_workspace_bytes(const moe_cfg* cfg);
  * moe_workspace_bytes(cfg). */
 int moe_workspace_init(const moe_cfg* cfg, void* ws, size_t ws_bytes, void* stream);
 
+/* One-time split of the fp32 router weights for the tensor-core router path:
+ *   W_r        fp32 [d, E]
+ *   W_r_split  bf16 [3, E, d] out: W_r[i][e] = hi + mid + lo exactly, with
+ *              hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid), stored
+ *              transposed (K-major) as W_r_split[0|1|2][e][i]. */
+int moe_pack_router(const moe_cfg* cfg, const float* W_r, moe_bf16* W_r_split, void* stream);
+
 /* Step 1, the router ("Expert parallelism", step 1 "Route": compute the
  * router for the local tokens).
  *   x          bf16 [T, d]
- *   W_r        fp32 [d, E]
+ *   W_r        fp32 [d, E], used when W_r_split is NULL (fp32 SIMT dot products)
+ *   W_r_split  bf16 [3, E, d] from moe_pack_router, or NULL.  When given, the
+ *              logits come from the tensor cores: x times each of the three
+ *              bf16 terms (every product exact in fp32), accumulated in fp32.
  *   logit_bias fp32 [E] or NULL: added to every token's logits
  *   scores     fp32 [T, E] out: logits l = x W_r (+ logit_bias), fp32
- *              accumulation; with MOE_SIGMOID the affinity 1/(1+exp(-l)). */
+ *              accumulation; with MOE_SIGMOID the affinity 1/(1+exp(-l)).
+ *   ws         workspace or NULL: receives MOE_E_DEVICE_TIMEOUT if a bounded
+ *              wait of the tensor-core path gives up. */
 int moe_router_logits(const moe_cfg* cfg, const moe_bf16* x, const float* W_r,
-                      const float* logit_bias, float* scores, void* stream);
+                      const moe_bf16* W_r_split, const float* logit_bias, float* scores,
+                      void* ws, size_t ws_bytes, void* stream);
 
 /* Step 1, top-k choice and gates ("Expert parallelism", step 1; node-limited
  * routing in "What DeepSeek-V3 did about it"; the selection bias of "05 -

@@ -63,21 +63,27 @@ def test_full_size_layer_on_sampled_tokens(m, name, n_sample):
     assert_y_close(npf(layer.y[torch.from_numpy(tokens).to(dev)]), y_ref[tokens])
 
 
-@pytest.mark.parametrize("name", ["mixtral", "dsv3", "skew"])
-def test_full_size_router_logits_on_sampled_tokens(m, name):
+@pytest.mark.parametrize("name,tc", [("mixtral", False), ("mixtral", True), ("dsv3", False),
+                                     ("dsv3", True), ("skew", True)])
+def test_full_size_router_logits_on_sampled_tokens(m, name, tc):
     cfg = synth.CONFIGS[name]
     dev = torch.device("cuda")
     x = synth.make_x(cfg, device=dev)
     W_r, lb = synth.make_router(cfg, device=dev)
     c = m.MoeCfg.from_layer(cfg)
     out = torch.empty(cfg.T, cfg.E, dtype=torch.float32, device=dev)
-    m.moe_router_logits(c, x, W_r, lb, out)
+    split = None
+    if tc:
+        split = torch.empty(3, cfg.E, cfg.d, dtype=torch.bfloat16, device=dev)
+        m.moe_pack_router(c, W_r, split)
+    m.moe_router_logits(c, x, None if tc else W_r, split, lb, out)
     torch.cuda.synchronize()
     tokens = synth.sample_tokens(cfg, 256).numpy()
     xs = x[torch.from_numpy(tokens).to(dev)].float().cpu().numpy()
     Wn = W_r.cpu().numpy()
     l_ref = oracle.router_logits(xs, Wn, None if lb is None else lb.cpu().numpy())
-    bound = cfg.d * 2.0 ** -24 * (np.abs(xs) @ np.abs(Wn)) + 2.0 ** -23 * np.abs(l_ref)
+    bound = ((3 if tc else 1) * cfg.d * 2.0 ** -24 * (np.abs(xs) @ np.abs(Wn))
+             + 2.0 ** -23 * np.abs(l_ref))
     got = npf(out[torch.from_numpy(tokens).to(dev)])
     if cfg.score_fn == "sigmoid":
         assert (np.abs(got - oracle.sigmoid(l_ref)) <= 0.25 * bound + 4e-7).all()

@@ -243,18 +243,30 @@ def _logit_bound(x, W):
     return d * 2.0 ** -24 * (np.abs(x) @ np.abs(W))
 
 
-@pytest.mark.parametrize("name", ["tiny", "ds_small", "skew_small", "k_equals_E"])
-def test_router_logits_parity(m, name):
+def _router_split(m, c, W_r_dev):
+    split = torch.empty(3, c.E, c.d, dtype=torch.bfloat16, device="cuda")
+    m.moe_pack_router(c, W_r_dev, split)
+    return split
+
+
+@pytest.mark.parametrize("name", ["tiny", "ds_small", "skew_small", "k_equals_E", "norm_softmax"])
+@pytest.mark.parametrize("tc", [False, True])
+def test_router_logits_parity(m, name, tc):
+    """fp32 SIMT path: bound d*u*sum|x_i w_i|.  Tensor-core path: 3d exact
+    products summed in fp32, bound 3*d*u*sum|x_i w_i|."""
     cfg = SMALL[name]
     x = synth.make_x(cfg)
     W_r, lb = synth.make_router(cfg)
     c = m.MoeCfg.from_layer(cfg)
     out = torch.empty(cfg.T, cfg.E, dtype=torch.float32, device="cuda")
-    m.moe_router_logits(c, x.cuda(), W_r.cuda(), None if lb is None else lb.cuda(), out)
+    W_dev = W_r.cuda()
+    split = _router_split(m, c, W_dev) if tc else None
+    m.moe_router_logits(c, x.cuda(), None if tc else W_dev, split,
+                        None if lb is None else lb.cuda(), out)
     torch.cuda.synchronize()
     xf, Wf = x.float().numpy(), W_r.numpy()
     l_ref = oracle.router_logits(xf, Wf, None if lb is None else lb.numpy())
-    bound = _logit_bound(xf, Wf) + 1e-30
+    bound = (3 if tc else 1) * _logit_bound(xf, Wf) + 1e-30
     got = npf(out)
     if cfg.score_fn == "sigmoid":
         s_ref = oracle.sigmoid(l_ref)
@@ -264,6 +276,16 @@ def test_router_logits_parity(m, name):
             bound = bound + 2.0 ** -24 * np.abs(l_ref)
         assert (np.abs(got - l_ref) <= bound).all()
         assert np.median(np.abs(got - l_ref)) < 1e-5
+
+
+def test_router_split_is_exact(m):
+    """hi + mid + lo reproduces every fp32 router weight exactly."""
+    cfg = SMALL["ds_small"]
+    W_r, _ = synth.make_router(cfg)
+    c = m.MoeCfg.from_layer(cfg)
+    split = _router_split(m, c, W_r.cuda()).double().cpu()
+    recon = (split[0] + split[1] + split[2]).T.numpy()
+    assert np.array_equal(recon, W_r.double().numpy())
 
 
 def test_layer_from_tokens_with_router(m):
