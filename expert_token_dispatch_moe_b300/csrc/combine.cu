@@ -43,24 +43,37 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
       rows[j] = __shfl_sync(0xffffffffu, my_row, j);
       gs[j] = __shfl_sync(0xffffffffu, my_g, j);
     }
-    for (int v = lane; v < vec; v += 32) {
-      uint4 val[KT > 0 ? KT : 1];
+    // U vectors per lane per pass: about 8 row loads in flight per lane
+    constexpr int U = KT <= 1 ? 8 : (KT <= 2 ? 4 : (KT <= 4 ? 2 : 1));
+    for (int v0 = lane; v0 < vec; v0 += 32 * U) {
+      uint4 val[U][KT > 0 ? KT : 1];
+      uint4 sv[U];
 #pragma unroll
-      for (int j = 0; j < KT; ++j)
-        if (rows[j] >= 0) val[j] = __ldg(y_sorted + size_t(rows[j]) * vec + v);
-      uint4 sv = make_uint4(0, 0, 0, 0);
-      if (has_shared) sv = __ldg(shared_row + v);
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + 32 * u;
+        if (v < vec) {
 #pragma unroll
-      for (int j = 0; j < KT; ++j)
-        if (rows[j] >= 0) fma_bf16x8(acc, val[j], gs[j]);
-      if (has_shared) fma_bf16x8(acc, sv, 1.0f);
-      uint4 o;
-      o.x = pack_bf16x2(acc[0], acc[1]);
-      o.y = pack_bf16x2(acc[2], acc[3]);
-      o.z = pack_bf16x2(acc[4], acc[5]);
-      o.w = pack_bf16x2(acc[6], acc[7]);
-      y[size_t(t) * vec + v] = o;
+          for (int j = 0; j < KT; ++j)
+            if (rows[j] >= 0) val[u][j] = __ldg(y_sorted + size_t(rows[j]) * vec + v);
+          if (has_shared) sv[u] = __ldg(shared_row + v);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + 32 * u;
+        if (v >= vec) break;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < KT; ++j)
+          if (rows[j] >= 0) fma_bf16x8(acc, val[u][j], gs[j]);
+        if (has_shared) fma_bf16x8(acc, sv[u], 1.0f);
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        y[size_t(t) * vec + v] = o;
+      }
     }
   } else {
     // warp-uniform trip count: every lane takes part in the broadcasts

@@ -14,17 +14,17 @@ namespace moe {
 
 // ---------------------------------------------------------------------------
 // Workspace layout (all regions 256-byte aligned)
-//   [0, 256)       status word (int32) + spare
+//   [0, 256)       status word (int32 at 0), finished-CTA counter of the
+//                  permute histogram (uint32 at 8, back to 0 after each call)
 //   src_cnt        int32 [n_ep][E]   assignments per (source rank, expert)
 //   chunk_hist     int32 [n_chunks][E] per-chunk histogram, then chunk bases
-//   ep_before      int32 [n_ep][E]   assignments to e from ranks < s
 //   ep_sbase       int32 [n_ep][E]   send-slot base for (s, e)
 //   send_pos       int32 [A]         send slot of each assignment (-1 dropped)
 // ---------------------------------------------------------------------------
 constexpr int kPermChunk = 2048;   // assignments per histogram/rank CTA
 
 struct WsLayout {
-  size_t status, src_cnt, chunk_hist, ep_before, ep_sbase, send_pos, total;
+  size_t status, done_ctas, src_cnt, chunk_hist, ep_sbase, send_pos, total;
   int n_chunks;
 };
 
@@ -35,10 +35,9 @@ inline WsLayout ws_layout(const moe_cfg& c) {
   size_t A = size_t(c.T) * c.k;
   L.n_chunks = int((A + kPermChunk - 1) / kPermChunk);
   size_t off = 0;
-  L.status = off;     off += 256;
+  L.status = off;     L.done_ctas = off + 8;  off += 256;
   L.src_cnt = off;    off += align256(size_t(c.n_ep) * c.E * 4);
   L.chunk_hist = off; off += align256(size_t(L.n_chunks) * c.E * 4);
-  L.ep_before = off;  off += align256(size_t(c.n_ep) * c.E * 4);
   L.ep_sbase = off;   off += align256(size_t(c.n_ep) * c.E * 4);
   L.send_pos = off;   off += align256(A * 4);
   L.total = off;
@@ -139,6 +138,15 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
       : "memory");
+}
+
+// Bring a tile into L2 ahead of its shared-memory load (no completion
+// tracking; out-of-range coordinates fetch nothing).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(c0), "r"(c1)
+               : "memory");
 }
 
 // ---------------------------------------------------------------------------

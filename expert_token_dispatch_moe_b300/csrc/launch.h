@@ -12,6 +12,9 @@ namespace moe {
 void reset_launches();
 void note_launches(int n);
 
+// Multiprocessors of the current device (cached per device; 148 if unknown).
+int device_sm_count();
+
 int launch_router_logits(const moe_cfg& c, const void* x, const float* W, const float* lbias,
                          float* out, cudaStream_t st);
 int launch_router_tc(const moe_cfg& c, const void* x, const void* W_split, const float* lbias,

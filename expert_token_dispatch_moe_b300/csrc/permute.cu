@@ -7,15 +7,16 @@
 // sums, never from the order of atomics, so every output is deterministic:
 //   1. hist:  per 2048-assignment chunk, a histogram over experts (shared-memory
 //             atomics: only counts, not order, depend on them); counts per
-//             (source rank, expert) for the layout.
-//   2. scan:  per expert, exclusive prefix over chunks (chunk bases), totals,
-//             and the exclusive prefix over experts (segment offsets).
-//   3. rank:  per chunk, warp-ordered match/popc ranks, giving each
+//             (source rank, expert) for the layout.  The CTA that finishes
+//             last then scans: per expert, the exclusive prefix over chunks
+//             (chunk bases) and totals, and the exclusive prefix over experts
+//             (segment offsets).
+//   2. rank:  per chunk, warp-ordered match/popc ranks, giving each
 //             assignment its row; writes inv and order.
-//   4. move:  one warp per token reads x[t] once (16-byte vectors) and writes
+//   3. move:  one warp per token reads x[t] once (16-byte vectors) and writes
 //             its k copies.
 // Capacity mode keeps rank < cap at row e*cap + rank and zero-fills the rest
-// of each segment.
+// of each segment (one warp per row, over the whole grouped buffer).
 #include "common.cuh"
 #include "launch.h"
 
@@ -25,78 +26,115 @@ constexpr int kPermThreads = 256;
 constexpr int kPermPerThread = kPermChunk / kPermThreads;  // 8
 
 // ---------------------------------------------------------------------------
-// 1. histogram
+// 1. histogram, then (last CTA) the scans
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kPermThreads) perm_hist_kernel(
-    const int32_t* __restrict__ idx, int A, int E, int k, int T_loc, int32_t* __restrict__ chunk_hist,
-    int32_t* __restrict__ src_cnt, int* status) {
-  extern __shared__ int32_t h[];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
-  __syncthreads();
-  const int base = blockIdx.x * kPermChunk;
-#pragma unroll
-  for (int i = 0; i < kPermPerThread; ++i) {
-    const int a = base + i * kPermThreads + threadIdx.x;
-    if (a < A) {
-      const int e = __ldg(idx + a);
-      if (e >= 0 && e < E) {
-        atomicAdd(&h[e], 1);
-        const int s = (a / k) / T_loc;
-        atomicAdd(&src_cnt[size_t(s) * E + e], 1);
-      } else {
-        report_status(status, MOE_E_DEVICE_DATA);
-      }
-    }
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_hist[size_t(blockIdx.x) * E + e] = h[e];
-}
-
-// ---------------------------------------------------------------------------
-// 2. scan (one CTA of 1024 threads; E <= 1024)
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ chunk_hist,
-                                                         int n_chunks, int E, int capacity,
-                                                         int32_t* __restrict__ counts,
-                                                         int32_t* __restrict__ offsets) {
-  __shared__ int32_t warp_tot[32];
-  const int e = threadIdx.x;
-  int total = 0;
-  if (e < E) {
-    for (int c = 0; c < n_chunks; ++c) {
-      const int v = chunk_hist[size_t(c) * E + e];
-      chunk_hist[size_t(c) * E + e] = total;  // becomes the chunk base
-      total += v;
-    }
-    counts[e] = total;
-  }
-  // exclusive block scan of totals over experts
+// Exclusive prefix over the E per-expert totals in tot[] (shared memory),
+// in place, by the whole CTA (kPermThreads threads, E <= 4 * kPermThreads).
+// Returns the sum of all totals.
+__device__ int block_exclusive_scan(int32_t* tot, int E) {
+  __shared__ int32_t warp_sum[kPermThreads / 32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = total;
+  const int e0 = threadIdx.x * 4;
+  int v[4], local = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[i] = (e0 + i < E) ? tot[e0 + i] : 0;
+    local += v[i];
+  }
+  int incl = local;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const int o = __shfl_up_sync(0xffffffffu, incl, off);
     if (lane >= off) incl += o;
   }
-  if (lane == 31) warp_tot[warp] = incl;
+  if (lane == 31) warp_sum[warp] = incl;
   __syncthreads();
-  if (warp == 0) {
-    int w = warp_tot[lane];
+  int before = 0, all = 0;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, w, off);
-      if (lane >= off) w += o;
-    }
-    warp_tot[lane] = w;  // inclusive over warps
+  for (int w = 0; w < kPermThreads / 32; ++w) {
+    if (w < warp) before += warp_sum[w];
+    all += warp_sum[w];
+  }
+  int run = before + incl - local;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (e0 + i < E) tot[e0 + i] = run;
+    run += v[i];
   }
   __syncthreads();
-  const int excl = incl - total + (warp > 0 ? warp_tot[warp - 1] : 0);
-  if (e < E) offsets[e] = capacity ? e * capacity : excl;
-  if (e == E - 1) offsets[E] = capacity ? E * capacity : excl + total;
+  return all;
+}
+
+__global__ void __launch_bounds__(kPermThreads) perm_hist_kernel(
+    const int32_t* __restrict__ idx, int A, int E, int k, int T_loc, int capacity,
+    int32_t* __restrict__ chunk_hist, int32_t* __restrict__ src_cnt, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int* status, unsigned int* done_ctas) {
+  extern __shared__ int32_t h[];  // [E]; reused by the last CTA for totals
+  __shared__ bool last;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int base = blockIdx.x * kPermChunk;
+#pragma unroll
+  for (int i = 0; i < kPermPerThread; ++i) {
+    const int a = base + i * kPermThreads + threadIdx.x;
+    int key = -1;
+    if (a < A) {
+      const int e = __ldg(idx + a);
+      if (e >= 0 && e < E) {
+        atomicAdd(&h[e], 1);
+        key = ((a / k) / T_loc) * E + e;
+      } else {
+        report_status(status, MOE_E_DEVICE_DATA);
+      }
+    }
+    // one global atomic per distinct (source rank, expert) in the warp
+    const uint32_t peers = __match_any_sync(0xffffffffu, key);
+    if (key >= 0 && (peers & ((1u << lane) - 1u)) == 0) atomicAdd(src_cnt + key, __popc(peers));
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_hist[size_t(blockIdx.x) * E + e] = h[e];
+
+  // The last CTA to finish turns the chunk histograms into chunk bases.
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(done_ctas, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const int n_chunks = gridDim.x;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int total = 0;
+    int c = 0;
+    for (; c + 4 <= n_chunks; c += 4) {
+      int v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = __ldcg(chunk_hist + size_t(c + u) * E + e);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        chunk_hist[size_t(c + u) * E + e] = total;  // becomes the chunk base
+        total += v[u];
+      }
+    }
+    for (; c < n_chunks; ++c) {
+      const int v = __ldcg(chunk_hist + size_t(c) * E + e);
+      chunk_hist[size_t(c) * E + e] = total;
+      total += v;
+    }
+    counts[e] = total;
+    h[e] = total;
+  }
+  __syncthreads();
+  const int all = block_exclusive_scan(h, E);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) offsets[e] = capacity ? e * capacity : h[e];
+  if (threadIdx.x == 0) {
+    offsets[E] = capacity ? E * capacity : all;
+    *done_ctas = 0u;  // ready for the next call
+  }
 }
 
 // ---------------------------------------------------------------------------
-// 3. stable ranks -> rows
+// 2. stable ranks -> rows
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kPermThreads) perm_rank_kernel(
     const int32_t* __restrict__ idx, int A, int E, int capacity,
@@ -155,7 +193,7 @@ __global__ void __launch_bounds__(kPermThreads) perm_rank_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// 4. row move: one warp per token, x[t] read once, written to its k rows.
+// 3. row move: one warp per token, x[t] read once, written to its k rows.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) row_scatter_kernel(const uint4* __restrict__ x, int T,
                                                           int vec_per_row, int k,
@@ -187,105 +225,133 @@ __global__ void __launch_bounds__(256) row_scatter_kernel(const uint4* __restric
   }
 }
 
-// Capacity mode: zero the unfilled rows of each expert segment, order = -1.
+// Capacity mode: zero the padding rows of the grouped buffer and set their
+// order entry to -1.  Row r belongs to expert e = r / cap and is padding when
+// r - e*cap >= min(counts[e], cap).  One warp per row, grid-stride.
 __global__ void __launch_bounds__(256) perm_pad_kernel(const int32_t* __restrict__ counts,
-                                                       int capacity, int vec_per_row,
+                                                       int capacity, int R, int vec_per_row,
                                                        int32_t* __restrict__ order,
                                                        uint4* __restrict__ x_sorted) {
-  const int e = blockIdx.x;
-  const int kept = min(__ldg(counts + e), capacity);
-  const int r0 = e * capacity + kept, r1 = (e + 1) * capacity;
-  for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) order[r] = -1;
-  const size_t n = size_t(r1 - r0) * vec_per_row;
-  uint4* base = x_sorted + size_t(r0) * vec_per_row;
-  for (size_t i = threadIdx.x; i < n; i += blockDim.x) base[i] = make_uint4(0, 0, 0, 0);
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < R; r += warps) {
+    const int e = r / capacity;
+    if (r - e * capacity < min(__ldg(counts + e), capacity)) continue;
+    if (lane == 0) order[r] = -1;
+    uint4* row = x_sorted + size_t(r) * vec_per_row;
+    for (int v = lane; v < vec_per_row; v += 32) row[v] = make_uint4(0, 0, 0, 0);
+  }
 }
 
 // ---------------------------------------------------------------------------
 // Expert-parallel layout
 // ---------------------------------------------------------------------------
-// One CTA: kept rows per (source s, expert e), C, send/recv offsets and the
-// send-slot base of each (s, e):  slot(a) = s*T_loc*k + sum_{e'<e} kept[s][e']
-//                                          + rank(a) - before[s][e]
-// where rank(a) is the assignment's stable rank in its expert and before[s][e]
-// the assignments to e from ranks < s (kept rows of a rank are a prefix of its
-// ranks in the expert).
-__global__ void __launch_bounds__(1024) ep_tables_kernel(
+// One CTA per source rank s.  With before[e] = assignments to e from ranks
+// < s (kept rows of a rank are a prefix of its ranks in the expert):
+//   kept[e]      = c[s][e], or clamp(cap - before[e], 0, c[s][e]) with a capacity
+//   sbase[s][e]  = s*T_loc*k + sum_{e'<e} kept[e'] - before[e], so that
+//                  slot(a) = sbase[s][e] + rank(a)
+//   C[s][q]      = sum of kept[e] over q's experts [q*G, (q+1)*G), G = E/n_ep
+//   send_off[s][q] = sum_{e<q*G} kept[e]
+//   recv_off[q][s] = rows q received from ranks < s
+//                  = sum over q's experts of before[e] (or min(before[e], cap)).
+__global__ void __launch_bounds__(kPermThreads) ep_tables_kernel(
     const int32_t* __restrict__ src_cnt, int n_ep, int E, int k, int T_loc, int capacity,
-    int32_t* __restrict__ before, int32_t* __restrict__ sbase, int32_t* __restrict__ C,
-    int32_t* __restrict__ send_off, int32_t* __restrict__ recv_off) {
-  // pass 1: per expert, over sources
+    int32_t* __restrict__ sbase, int32_t* __restrict__ C, int32_t* __restrict__ send_off,
+    int32_t* __restrict__ recv_off) {
+  extern __shared__ int32_t sm[];
+  int32_t* kept = sm;              // [E + 1] -> exclusive prefix
+  int32_t* recv = sm + E + 1;      // [E + 1] -> exclusive prefix
+  int32_t* bef = sm + 2 * (E + 1); // [E]
+  const int s = blockIdx.x;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int s = 0; s < n_ep; ++s) {
-      const int c = src_cnt[size_t(s) * E + e];
-      before[size_t(s) * E + e] = run;
-      int kept = c;
-      if (capacity) kept = max(0, min(capacity - run, c));
-      sbase[size_t(s) * E + e] = kept;  // temporarily: kept count
-      run += c;
+    int b = 0, sp = 0;
+    for (; sp + 4 <= s; sp += 4) {
+      int v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = __ldg(src_cnt + size_t(sp + u) * E + e);
+      b += v[0] + v[1] + v[2] + v[3];
     }
+    for (; sp < s; ++sp) b += __ldg(src_cnt + size_t(sp) * E + e);
+    const int c = __ldg(src_cnt + size_t(s) * E + e);
+    kept[e] = capacity ? max(0, min(capacity - b, c)) : c;
+    recv[e] = capacity ? min(b, capacity) : b;
+    bef[e] = b;
   }
   __syncthreads();
-  // pass 2: per source, over experts (destination = e * n_ep / E, monotone in e)
-  for (int s = threadIdx.x; s < n_ep; s += blockDim.x) {
-    int run = 0;
-    for (int q = 0; q < n_ep; ++q) C[size_t(s) * n_ep + q] = 0;
-    for (int e = 0; e < E; ++e) {
-      const int kept = sbase[size_t(s) * E + e];
-      sbase[size_t(s) * E + e] = s * T_loc * k + run - before[size_t(s) * E + e];
-      C[size_t(s) * n_ep + (e * n_ep) / E] += kept;
-      run += kept;
-    }
-    int o = 0;
-    for (int q = 0; q < n_ep; ++q) {
-      send_off[size_t(s) * n_ep + q] = o;
-      o += C[size_t(s) * n_ep + q];
-    }
+  const int kept_all = block_exclusive_scan(kept, E);
+  const int recv_all = block_exclusive_scan(recv, E);
+  if (threadIdx.x == 0) {
+    kept[E] = kept_all;
+    recv[E] = recv_all;
   }
   __syncthreads();
+  const int base = s * T_loc * k;
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    sbase[size_t(s) * E + e] = base + kept[e] - bef[e];
+  const int G = E / n_ep;
   for (int q = threadIdx.x; q < n_ep; q += blockDim.x) {
-    int o = 0;
-    for (int s = 0; s < n_ep; ++s) {
-      recv_off[size_t(q) * n_ep + s] = o;
-      o += C[size_t(s) * n_ep + q];
-    }
+    C[size_t(s) * n_ep + q] = kept[(q + 1) * G] - kept[q * G];
+    send_off[size_t(s) * n_ep + q] = kept[q * G];
+    recv_off[size_t(q) * n_ep + s] = recv[(q + 1) * G] - recv[q * G];
   }
 }
 
+// Per assignment a: its send slot (send_pos[a], -1 when dropped) and
+// send_idx[slot] = a.  Thread p also marks slot p empty (send_idx = -1) when
+// it lies past its rank's kept rows (capacity drops, or invalid expert ids).
 __global__ void __launch_bounds__(256) ep_scatter_kernel(
     const int32_t* __restrict__ idx, const int32_t* __restrict__ inv,
-    const int32_t* __restrict__ offsets, const int32_t* __restrict__ sbase, int A, int E, int k,
-    int T_loc, int32_t* __restrict__ send_idx, int32_t* __restrict__ send_pos) {
+    const int32_t* __restrict__ offsets, const int32_t* __restrict__ sbase,
+    const int32_t* __restrict__ C, const int32_t* __restrict__ send_off, int A, int E, int k,
+    int T_loc, int n_ep, int32_t* __restrict__ send_idx, int32_t* __restrict__ send_pos) {
   const int a = blockIdx.x * blockDim.x + threadIdx.x;
   if (a >= A) return;
   const int e = __ldg(idx + a);
   const int row = __ldg(inv + a);
+  const int rpr = T_loc * k;
+  const int s = a / rpr;
   int p = -1;
   if (row >= 0 && e >= 0 && e < E) {
     const int rank = row - __ldg(offsets + e);
-    const int s = (a / k) / T_loc;
     p = __ldg(sbase + size_t(s) * E + e) + rank;
     send_idx[p] = a;
   }
   send_pos[a] = p;
+  const size_t last = size_t(s) * n_ep + n_ep - 1;
+  const int used = __ldg(send_off + last) + __ldg(C + last);
+  if (a - s * rpr >= used) send_idx[a] = -1;
 }
 
-// Capacity mode: zero the send-buffer rows past each rank's kept rows.
-__global__ void __launch_bounds__(256) ep_pad_kernel(const int32_t* __restrict__ C, int n_ep,
-                                                     int rows_per_rank, int vec_per_row,
+// Zero the send-buffer rows past each rank's kept rows (slot p of rank
+// s = p / rows_per_rank is empty when p - s*rows_per_rank >= its kept rows).
+// One warp per row, grid-stride.
+__global__ void __launch_bounds__(256) ep_pad_kernel(const int32_t* __restrict__ C,
+                                                     const int32_t* __restrict__ send_off,
+                                                     int n_ep, int rows_per_rank, int A,
+                                                     int vec_per_row,
                                                      uint4* __restrict__ send_buf) {
-  const int s = blockIdx.x;
-  int used = 0;
-  for (int q = 0; q < n_ep; ++q) used += __ldg(C + size_t(s) * n_ep + q);
-  const size_t n = size_t(rows_per_rank - used) * vec_per_row;
-  uint4* base = send_buf + (size_t(s) * rows_per_rank + used) * vec_per_row;
-  for (size_t i = threadIdx.x; i < n; i += blockDim.x) base[i] = make_uint4(0, 0, 0, 0);
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int p = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; p < A; p += warps) {
+    const int s = p / rows_per_rank;
+    const size_t last = size_t(s) * n_ep + n_ep - 1;
+    if (p - s * rows_per_rank < __ldg(send_off + last) + __ldg(C + last)) continue;
+    uint4* row = send_buf + size_t(p) * vec_per_row;
+    for (int v = lane; v < vec_per_row; v += 32) row[v] = make_uint4(0, 0, 0, 0);
+  }
 }
 
 // ---------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------
+// Blocks of 256 threads for a grid-stride pass with one warp per row.
+static int row_grid(long long rows) {
+  const long long want = (rows + 7) / 8;
+  const long long cap = 8LL * device_sm_count();
+  return int(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
 int launch_row_scatter(const void* x, int T, int d, int k, const int32_t* rows, void* dst,
                        cudaStream_t st) {
   const int vec = d / 8;  // 16-byte vectors per row
@@ -301,18 +367,20 @@ int launch_permute(const moe_cfg& c, const void* x, const int32_t* idx, int32_t*
   const WsLayout L = ws_layout(c);
   const int A = c.T * c.k;
   int32_t* status = ws_ptr<int32_t>(ws, L.status);
+  unsigned int* done = ws_ptr<unsigned int>(ws, L.done_ctas);
   int32_t* src_cnt = ws_ptr<int32_t>(ws, L.src_cnt);
   int32_t* chunk_hist = ws_ptr<int32_t>(ws, L.chunk_hist);
   if (cudaMemsetAsync(src_cnt, 0, size_t(c.n_ep) * c.E * 4, st) != cudaSuccess) return MOE_E_CUDA;
-  perm_hist_kernel<<<L.n_chunks, kPermThreads, c.E * 4, st>>>(idx, A, c.E, c.k, c.T / c.n_ep,
-                                                              chunk_hist, src_cnt, status);
-  perm_scan_kernel<<<1, 1024, 0, st>>>(chunk_hist, L.n_chunks, c.E, c.capacity, counts, offsets);
+  perm_hist_kernel<<<L.n_chunks, kPermThreads, c.E * 4, st>>>(
+      idx, A, c.E, c.k, c.T / c.n_ep, c.capacity, chunk_hist, src_cnt, counts, offsets, status,
+      done);
   perm_rank_kernel<<<L.n_chunks, kPermThreads, 8 * c.E * 4, st>>>(idx, A, c.E, c.capacity,
                                                                   chunk_hist, offsets, inv, order);
-  note_launches(3);
+  note_launches(2);
   if (c.capacity) {
-    perm_pad_kernel<<<c.E, 256, 0, st>>>(counts, c.capacity, c.d / 8, order,
-                                         static_cast<uint4*>(x_sorted));
+    const int R = c.E * c.capacity;
+    perm_pad_kernel<<<row_grid(R), 256, 0, st>>>(counts, c.capacity, R, c.d / 8, order,
+                                                 static_cast<uint4*>(x_sorted));
     note_launches(1);
   }
   if (cudaGetLastError() != cudaSuccess) return MOE_E_CUDA;
@@ -327,21 +395,19 @@ int launch_ep_layout(const moe_cfg& c, const int32_t* idx, const int32_t* offset
   const int A = c.T * c.k;
   const int T_loc = c.T / c.n_ep;
   int32_t* src_cnt = ws_ptr<int32_t>(ws, L.src_cnt);
-  int32_t* before = ws_ptr<int32_t>(ws, L.ep_before);
   int32_t* sbase = ws_ptr<int32_t>(ws, L.ep_sbase);
   int32_t* send_pos = ws_ptr<int32_t>(ws, L.send_pos);
-  if (c.capacity && cudaMemsetAsync(send_idx, 0xff, size_t(A) * 4, st) != cudaSuccess)
-    return MOE_E_CUDA;
-  ep_tables_kernel<<<1, 1024, 0, st>>>(src_cnt, c.n_ep, c.E, c.k, T_loc, c.capacity, before,
-                                       sbase, C, send_off, recv_off);
-  ep_scatter_kernel<<<(A + 255) / 256, 256, 0, st>>>(idx, inv, offsets, sbase, A, c.E, c.k, T_loc,
-                                                     send_idx, send_pos);
+  const size_t smem = size_t(3 * c.E + 2) * 4;
+  ep_tables_kernel<<<c.n_ep, kPermThreads, smem, st>>>(src_cnt, c.n_ep, c.E, c.k, T_loc,
+                                                       c.capacity, sbase, C, send_off, recv_off);
+  ep_scatter_kernel<<<(A + 255) / 256, 256, 0, st>>>(idx, inv, offsets, sbase, C, send_off, A,
+                                                     c.E, c.k, T_loc, c.n_ep, send_idx, send_pos);
   note_launches(2);
   if (cudaGetLastError() != cudaSuccess) return MOE_E_CUDA;
   if (x && send_buf) {
     if (c.capacity) {
-      ep_pad_kernel<<<c.n_ep, 256, 0, st>>>(C, c.n_ep, T_loc * c.k, c.d / 8,
-                                            static_cast<uint4*>(send_buf));
+      ep_pad_kernel<<<row_grid(A), 256, 0, st>>>(C, send_off, c.n_ep, T_loc * c.k, A, c.d / 8,
+                                                 static_cast<uint4*>(send_buf));
       note_launches(1);
     }
     return launch_row_scatter(x, c.T, c.d, c.k, send_pos, send_buf, st);

@@ -66,10 +66,11 @@ MOE_API int moe_permute_noalloc(const moe_cfg* c, const moe_bf16* x, const int32
     if (!p) return MOE_E_NULL;
     if (reinterpret_cast<uintptr_t>(p) & 15u) return MOE_E_ALIGN;
   }
-  // The permute touches the status word, the per-(rank, expert) counts and the
-  // per-chunk histograms: the workspace regions that precede the EP tables.
+  // The permute touches the status word and histogram counter, the per-(rank,
+  // expert) counts and the per-chunk histograms: the workspace regions that
+  // precede the EP tables.
   const WsLayout L = ws_layout(*c);
-  if (L.ep_before > kNoallocScratchBytes) return MOE_E_SCRATCH_LIMIT;
+  if (L.ep_sbase > kNoallocScratchBytes) return MOE_E_SCRATCH_LIMIT;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
     cudaGetLastError();
@@ -86,7 +87,8 @@ MOE_API int moe_permute_noalloc(const moe_cfg* c, const moe_bf16* x, const int32
   void* ws = scratch_address(dev, &err);
   if (!ws) return err;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the status word must start at zero (the counters are cleared by the permute)
+  // the status word and the histogram's finished-CTA counter must start at zero
+  // (the per-(rank, expert) counts are cleared by the permute)
   if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) return MOE_E_CUDA;
   return launch_permute(*c, x, topk_idx, counts, offsets, order, inv, x_sorted, ws, st);
 }

@@ -57,18 +57,17 @@ __global__ void __launch_bounds__(256) route_topk_kernel(
   if (n_groups > 1) {
     const int gs = E / n_groups;
     uint32_t my_gkey = 0u;  // lane g holds group g's score key
-    for (int g = 0; g < n_groups; ++g) {
+    const int lpg = gs / EPL;  // lanes per group when groups are whole lanes
+    if (gs % EPL == 0 && (lpg & (lpg - 1)) == 0) {
+      // each lane's local top-2, then a reduction inside each aligned run of
+      // lpg lanes (xor offsets below lpg never leave the run)
       uint32_t t1 = 0u, t2 = 0u;
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
-        const int e = lane * EPL + i;
-        if (e < E && e / gs == g) {
-          const uint32_t kk = key[i];
-          if (kk > t1) { t2 = t1; t1 = kk; } else if (kk > t2) { t2 = kk; }
-        }
+        const uint32_t kk = key[i];
+        if (kk > t1) { t2 = t1; t1 = kk; } else if (kk > t2) { t2 = kk; }
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
+      for (int off = 1; off < lpg; off <<= 1) {
         const uint32_t o1 = __shfl_xor_sync(0xffffffffu, t1, off);
         const uint32_t o2 = __shfl_xor_sync(0xffffffffu, t2, off);
         const uint32_t hi = max(t1, o1), lo = min(t1, o1);
@@ -76,7 +75,31 @@ __global__ void __launch_bounds__(256) route_topk_kernel(
         t2 = max(lo, max(t2, o2));
       }
       const float gsum = __fadd_rn(key_value(t1), key_value(t2));
-      if (lane == g) my_gkey = order_key(gsum);
+      const uint32_t gk = order_key(gsum);
+      const uint32_t from = __shfl_sync(0xffffffffu, gk, (lane * lpg) & 31);
+      if (lane < n_groups) my_gkey = from;
+    } else {
+      for (int g = 0; g < n_groups; ++g) {
+        uint32_t t1 = 0u, t2 = 0u;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+          const int e = lane * EPL + i;
+          if (e < E && e / gs == g) {
+            const uint32_t kk = key[i];
+            if (kk > t1) { t2 = t1; t1 = kk; } else if (kk > t2) { t2 = kk; }
+          }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const uint32_t o1 = __shfl_xor_sync(0xffffffffu, t1, off);
+          const uint32_t o2 = __shfl_xor_sync(0xffffffffu, t2, off);
+          const uint32_t hi = max(t1, o1), lo = min(t1, o1);
+          t1 = hi;
+          t2 = max(lo, max(t2, o2));
+        }
+        const float gsum = __fadd_rn(key_value(t1), key_value(t2));
+        if (lane == g) my_gkey = order_key(gsum);
+      }
     }
     uint32_t kept = 0u;
     for (int r = 0; r < topk_groups; ++r) {
