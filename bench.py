@@ -400,9 +400,18 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--override", default="",
+                    help="comma-separated field=value changes to the workload, e.g. "
+                         "T=1024,E=32,n_ep=8 (a reduced case of the same shape for profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     cfg = synth.CONFIGS[args.config]
+    if args.override:
+        kw = {}
+        for item in args.override.split(","):
+            key, val = item.split("=")
+            kw[key.strip()] = type(getattr(cfg, key.strip()))(val)
+        cfg = cfg.with_(name=cfg.name + "[" + args.override + "]", **kw)
     if args.impl == "reference":
         run_reference(args, cfg)
     else:

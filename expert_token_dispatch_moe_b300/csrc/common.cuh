@@ -140,15 +140,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-// Bring a tile into L2 ahead of its shared-memory load (no completion
-// tracking; out-of-range coordinates fetch nothing).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int c0, int c1) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(m)),
-               "r"(c0), "r"(c1)
-               : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // tcgen05: tensor memory allocation, MMA, commit, loads
 // ---------------------------------------------------------------------------

@@ -8,7 +8,11 @@
 //               128-byte swizzle) into a 4-stage shared-memory ring
 //   warp 1      MMA issuer (one thread): tcgen05.mma kind::f16, M=128 N=256
 //               K=16, fp32 accumulators in tensor memory (two 256-column
-//               buffers, so the epilogue of one tile overlaps the next)
+//               buffers, so the epilogue of one tile overlaps the next).
+//               A segment's last M block with at most 64 valid rows is a
+//               half tile: 64-row A loads and M=64 MMAs (same issue time as
+//               M=128 but half the tensor work, which matters when the clock
+//               is held down by the power limit).
 //   warps 2-5   epilogue: tcgen05.ld of the accumulator, SwiGLU (GEMM 1) or
 //               plain conversion (GEMM 2), bf16 stores of the valid rows
 // Tiles come from a device-side schedule built from the expert counts and
@@ -110,9 +114,13 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Gr
   }
 }
 
+// tmA / tmA_sh: 128-row A boxes; tmA64 / tmA_sh64: the same tensors with 64-row
+// boxes for half tiles.
 __global__ void __launch_bounds__(gg::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmA_sh,
+                        const __grid_constant__ CUtensorMap tmA64,
+                        const __grid_constant__ CUtensorMap tmA_sh64,
                         const __grid_constant__ CUtensorMap tmB, const GroupedParams p) {
   using namespace gg;
   extern __shared__ uint8_t dyn_smem[];
@@ -179,6 +187,8 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmA_sh);
+    tma_prefetch_desc(&tmA64);
+    tma_prefetch_desc(&tmA_sh64);
     tma_prefetch_desc(&tmB);
   }
   tc_fence_before();
@@ -201,6 +211,8 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
     n_blk = local / m_tiles;
     m_blk = local - n_blk * m_tiles;
   };
+  // a half tile: the segment's last M block holds at most 64 valid rows
+  auto is_half = [&](int rows, int m_blk) { return rows - m_blk * BM <= BM / 2; };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -211,8 +223,10 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         int g, m_blk, n_blk, rows, a_row0, out_row0;
         decode(t, g, m_blk, n_blk, rows, a_row0, out_row0);
-        const CUtensorMap* ma =
-            (p.counts && g >= p.E && p.shared_a_separate) ? &tmA_sh : &tmA;
+        const bool sep = p.counts && g >= p.E && p.shared_a_separate;
+        const bool half = is_half(rows, m_blk);
+        const CUtensorMap* ma = half ? (sep ? &tmA_sh64 : &tmA64) : (sep ? &tmA_sh : &tmA);
+        const uint32_t tx = half ? A_BYTES / 2 + B_BYTES : STAGE_BYTES;
         const int a_row = a_row0 + m_blk * BM;
         const int b_row = g * p.N + n_blk * BN;
         for (int kb = 0; kb < num_kb; ++kb) {
@@ -221,7 +235,7 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
           uint8_t* sb = sa + A_BYTES;
           const int pass = kb / kb_per_pass;
           const int ka = (kb - pass * kb_per_pass) * BK;
-          mbar_arrive_expect_tx(&ctl.full[stage], STAGE_BYTES);
+          mbar_arrive_expect_tx(&ctl.full[stage], tx);
           tma_load_2d(sa, ma, ka, a_row, &ctl.full[stage]);
           tma_load_2d(sb, &tmB, ka, b_row + pass * p.b_pass_rows, &ctl.full[stage]);
           issued |= 1u << stage;
@@ -245,10 +259,13 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      const uint32_t idesc = idesc_bf16_f32(BM, BN);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        int g, m_blk, n_blk, rows, a_row0, out_row0;
+        decode(t, g, m_blk, n_blk, rows, a_row0, out_row0);
+        const uint32_t idesc = is_half(rows, m_blk) ? idesc_bf16_f32(BM / 2, BN)
+                                                    : idesc_bf16_f32(BM, BN);
         if (!wait_or_abort(&ctl.acc_empty[acc], acc_phase ^ 1u, ctl, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
@@ -275,8 +292,10 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
     }
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
-    const int quarter = warp & 3;  // tensor-memory lanes this warp may access
-    const int row_in_tile = quarter * 32 + lane;
+    // Warp w may access tensor-memory lanes [32*(w%4), 32*(w%4)+32).  An M=128
+    // accumulator keeps row r in lane r; an M=64 accumulator keeps rows
+    // 16q..16q+15 in lanes 32q..32q+15.
+    const int quarter = warp & 3;
     uint32_t acc = 0, acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       int g, m_blk, n_blk, rows, a_row0, out_row0;
@@ -284,8 +303,9 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
       if (!wait_or_abort(&ctl.acc_full[acc], acc_phase, ctl, p.status)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + acc * BN + (uint32_t(quarter * 32) << 16);
-      const int r = m_blk * BM + row_in_tile;
-      const bool valid = r < rows;
+      const bool half = is_half(rows, m_blk);
+      const int r = m_blk * BM + (half ? quarter * 16 + lane : quarter * 32 + lane);
+      const bool valid = (!half || lane < 16) && r < rows;
       const size_t orow_idx = size_t(out_row0 + (valid ? r : 0)) * p.ld_out;
       __nv_bfloat16* orow = p.out + orow_idx;
       if (p.mode == kEpiF32) {
@@ -453,8 +473,9 @@ int launch_router_tc(const moe_cfg& c, const void* x, const void* W_split, const
   using namespace gg;
   if (!get_encoder()) return MOE_E_CUDA;
   if (set_smem_attr() != MOE_OK) return MOE_E_CUDA;
-  CUtensorMap mA, mB;
+  CUtensorMap mA, mA64, mB;
   if (!make_map(&mA, x, uint64_t(c.T), c.d, BM)) return MOE_E_CUDA;
+  if (!make_map(&mA64, x, uint64_t(c.T), c.d, BM / 2)) return MOE_E_CUDA;
   if (!make_map(&mB, W_split, uint64_t(3) * c.E, c.d, BN)) return MOE_E_CUDA;
   const int sms = sm_count();
   if (sms <= 0) return MOE_E_CUDA;
@@ -473,7 +494,7 @@ int launch_router_tc(const moe_cfg& c, const void* x, const void* W_split, const
   p.status = status;
   const long long tiles = (long long)((c.T + BM - 1) / BM) * ((c.E + BN - 1) / BN);
   const int grid = int(tiles < sms ? tiles : sms);
-  grouped_gemm_kernel<<<grid, THREADS, DYN_SMEM, st>>>(mA, mA, mB, p);
+  grouped_gemm_kernel<<<grid, THREADS, DYN_SMEM, st>>>(mA, mA, mA64, mA64, mB, p);
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_E_CUDA;
 }
@@ -518,13 +539,16 @@ int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
   const int n_exp = c.E + c.has_shared;
   const uint64_t rows_h = uint64_t(R) + (c.has_shared ? c.T : 0);
 
-  CUtensorMap mA1, mA1s, mB1, mA2, mB2;
+  CUtensorMap mA1, mA1s, mA1h, mA1sh, mB1, mA2, mA2h, mB2;
+  const void* a1s = c.has_shared ? x : x_sorted;
+  const uint64_t a1s_rows = c.has_shared ? uint64_t(c.T) : uint64_t(R);
   if (!make_map(&mA1, x_sorted, uint64_t(R), c.d, BM)) return MOE_E_CUDA;
-  if (!make_map(&mA1s, c.has_shared ? x : x_sorted, c.has_shared ? uint64_t(c.T) : uint64_t(R),
-                c.d, BM))
-    return MOE_E_CUDA;
+  if (!make_map(&mA1h, x_sorted, uint64_t(R), c.d, BM / 2)) return MOE_E_CUDA;
+  if (!make_map(&mA1s, a1s, a1s_rows, c.d, BM)) return MOE_E_CUDA;
+  if (!make_map(&mA1sh, a1s, a1s_rows, c.d, BM / 2)) return MOE_E_CUDA;
   if (!make_map(&mB1, W13, uint64_t(n_exp) * 2 * c.f, c.d, BN)) return MOE_E_CUDA;
   if (!make_map(&mA2, h, rows_h, c.f, BM)) return MOE_E_CUDA;
+  if (!make_map(&mA2h, h, rows_h, c.f, BM / 2)) return MOE_E_CUDA;
   if (!make_map(&mB2, W2, uint64_t(n_exp) * c.d, c.f, BN)) return MOE_E_CUDA;
 
   // grid: at most one CTA per SM, no more than an upper bound on the tiles
@@ -550,7 +574,7 @@ int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
   p1.status = ws_ptr<int>(ws, L.status);
   const long long t1 = mt_ub * ((p1.N + BN - 1) / BN);
   const int grid1 = int(t1 < sms ? t1 : sms);
-  grouped_gemm_kernel<<<grid1, THREADS, DYN_SMEM, st>>>(mA1, mA1s, mB1, p1);
+  grouped_gemm_kernel<<<grid1, THREADS, DYN_SMEM, st>>>(mA1, mA1s, mA1h, mA1sh, mB1, p1);
 
   GroupedParams p2 = p1;
   p2.K = c.f;
@@ -561,7 +585,7 @@ int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
   p2.ld_out = c.d;
   const long long t2 = mt_ub * ((p2.N + BN - 1) / BN);
   const int grid2 = int(t2 < sms ? t2 : sms);
-  grouped_gemm_kernel<<<grid2, THREADS, DYN_SMEM, st>>>(mA2, mA2, mB2, p2);
+  grouped_gemm_kernel<<<grid2, THREADS, DYN_SMEM, st>>>(mA2, mA2, mA2h, mA2h, mB2, p2);
   note_launches(2);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_E_CUDA;
 }
