@@ -19,6 +19,7 @@ __all__ = [
     "capacity_rows", "permute", "ep_layout", "swiglu_expert",
     "expert_outputs", "combine", "moe_forward", "dense_mask_forward",
     "imbalance_eta", "alltoall_bytes", "dispatch_combine_bytes_per_token",
+    "bias_update", "eplb_replicate", "eplb_pack", "eplb_plan", "eplb_dispatch",
 ]
 
 F64 = np.float64
@@ -357,3 +358,107 @@ def dispatch_combine_bytes_per_token(k, d, s_disp, s_comb):
     k*d*(s_disp + s_comb) bytes ([EPM] "The all-to-all pattern": 2 x top_k x
     hidden x bytes)."""
     return k * d * (s_disp + s_comb)
+
+
+# ----------------------------------------------------------------------------
+# Load balancing: the auxiliary-loss-free bias update ([EPM] "Load balancing"
+# (b)) and redundant experts placed by replicate-then-pack ([EP] "Load
+# imbalance becomes idle time")
+# ----------------------------------------------------------------------------
+
+def bias_update(bias, counts, lr):
+    """One step of the bias control loop: after a step, count the tokens each
+    expert received; an under-loaded expert's selection bias rises and an
+    over-loaded one's falls, in proportion to its distance from the average
+    load over the experts ([EPM] "Load balancing" (b)).  fp64."""
+    c = np.asarray(counts, F64)
+    return np.asarray(bias, F64) + float(lr) * (c.mean() - c)
+
+
+def eplb_replicate(loads, n_slots):
+    """Step 1, Replicate: with n_slots expert slots in the group and E experts,
+    the n_slots - E spare slots are handed out one at a time, each to the expert
+    whose load per copy c_i / q_i is currently the largest (equal ratios: the
+    lower expert index).  Ratios are compared exactly as fractions.  Returns
+    q, the number of copies of every expert."""
+    from fractions import Fraction
+    c = [int(v) for v in loads]
+    E = len(c)
+    if n_slots < E:
+        raise ValueError("fewer slots than experts")
+    q = [1] * E
+    for _ in range(n_slots - E):
+        best = max(range(E), key=lambda i: (Fraction(c[i], q[i]), -i))
+        q[best] += 1
+    return np.array(q, np.int64)
+
+
+def eplb_pack(loads, q, n_ranks, slots):
+    """Step 2, Pack (longest processing time first): every copy of expert i
+    carries c_i / q_i; the copies, sorted by that load (largest first; equal
+    loads: lower expert index, then lower copy index), are placed one at a time
+    on the rank with the smallest load so far among those with a free slot
+    (equal loads: the lower rank).  Rank loads are fp64 sums of c_i / q_i in
+    placement order.
+
+    Returns (copy_rank, slot_expert, rank_load): copy_rank[off_i + j] = rank of
+    copy j of expert i (off = exclusive prefix of q); slot_expert[r][s] = the
+    expert in rank r's s-th filled slot, -1 when empty; rank_load[r] fp64."""
+    from fractions import Fraction
+    c = [int(v) for v in loads]
+    q = [int(v) for v in q]
+    E = len(c)
+    order = sorted(range(E), key=lambda i: (-Fraction(c[i], q[i]), i))
+    off = np.concatenate([[0], np.cumsum(q)])[:-1]
+    copy_rank = np.full(int(sum(q)), -1, np.int64)
+    slot_expert = np.full((n_ranks, slots), -1, np.int64)
+    used = [0] * n_ranks
+    load = [0.0] * n_ranks
+    for i in order:
+        per = float(c[i]) / float(q[i])
+        for j in range(q[i]):
+            free = [r for r in range(n_ranks) if used[r] < slots]
+            r = min(free, key=lambda rr: (load[rr], rr))
+            copy_rank[off[i] + j] = r
+            slot_expert[r][used[r]] = i
+            used[r] += 1
+            load[r] = load[r] + per
+    return copy_rank, slot_expert, np.array(load, F64)
+
+
+def eplb_plan(loads, n_ranks, slots):
+    """Replicate then pack ([EP] "Load imbalance becomes idle time")."""
+    q = eplb_replicate(loads, n_ranks * slots)
+    copy_rank, slot_expert, rank_load = eplb_pack(loads, q, n_ranks, slots)
+    return {"copies": q, "copy_offset": np.concatenate([[0], np.cumsum(q)])[:-1],
+            "copy_rank": copy_rank, "slot_expert": slot_expert, "rank_load": rank_load}
+
+
+def eplb_dispatch(idx, inv, offsets, counts, plan, n_ranks, T, capacity=0):
+    """Where every assignment goes once experts have copies: expert e's kept
+    assignments, in their stable order (rank r = inv[a] - offsets[e]), are
+    split evenly among its q_e copies, copy j taking ranks
+    [floor(j*m/q_e), floor((j+1)*m/q_e)) of its m kept assignments.  Returns
+    (dest_rank[A], C[s][g]) with s = the source rank of the token (T/n_ranks
+    tokens each) and g the rank holding that copy; dropped assignments get -1."""
+    idx = np.asarray(idx).reshape(-1)
+    inv = np.asarray(inv).reshape(-1)
+    A = idx.size
+    k = A // T
+    T_loc = T // n_ranks
+    dest = np.full(A, -1, np.int64)
+    C = np.zeros((n_ranks, n_ranks), np.int64)
+    for a in range(A):
+        if inv[a] < 0:
+            continue
+        e = int(idx[a])
+        r = int(inv[a]) - int(offsets[e])
+        m = int(counts[e]) if not capacity else min(int(counts[e]), capacity)
+        qe = int(plan["copies"][e])
+        j = 0
+        while (j + 1) * m // qe <= r:   # copy j holds ranks [j*m//qe, (j+1)*m//qe)
+            j += 1
+        g = int(plan["copy_rank"][int(plan["copy_offset"][e]) + j])
+        dest[a] = g
+        C[(a // k) // T_loc, g] += 1
+    return dest, C
