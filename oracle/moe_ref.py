@@ -20,6 +20,8 @@ __all__ = [
     "expert_outputs", "combine", "moe_forward", "dense_mask_forward",
     "imbalance_eta", "alltoall_bytes", "dispatch_combine_bytes_per_token",
     "bias_update", "eplb_replicate", "eplb_pack", "eplb_plan", "eplb_dispatch",
+    "E4M3_MAX", "e4m3_encode", "e4m3_decode", "quantize_rows_fp8", "dequantize_rows_fp8",
+    "ep_layout_fp8",
 ]
 
 F64 = np.float64
@@ -462,3 +464,87 @@ def eplb_dispatch(idx, inv, offsets, counts, plan, n_ranks, T, capacity=0):
         dest[a] = g
         C[(a // k) // T_loc, g] += 1
     return dest, C
+
+
+# ----------------------------------------------------------------------------
+# FP8 dispatch ([EP] "A worked example at DeepSeek-V3's shape": DeepSeek-V3
+# dispatches in FP8, s = 1 byte, and combines in BF16; "Lower precision on the
+# wire": FP8 halves s_disp).  The pages fix neither the FP8 format nor the
+# scale granularity: this restatement uses e4m3 (1 sign, 4 exponent bits with
+# bias 7, 3 mantissa bits; largest finite value 448) with one fp32 scale per
+# dispatched row, scale = absmax(row) / 448, code = e4m3(x / scale), rounding
+# to nearest even and saturating at +-448.  Floating-point steps are fp32, as
+# on the device, because they decide integer codes.
+# ----------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def e4m3_encode(v):
+    """fp32 values -> e4m3 codes (uint8), round to nearest even, saturate to
+    the largest finite magnitude 448 (NaN is not expected)."""
+    v = np.asarray(v, F32).astype(F64)          # exact
+    sign = (np.signbit(v)).astype(np.uint8) << 7
+    a = np.abs(v)
+    # quantum of the e4m3 grid around |v|: 2^(e-3) for normals (e >= -6), 2^-9 below
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, -6.0)
+    q = np.exp2(e - 3.0)
+    g = np.rint(a / q) * q                      # half to even (exact in fp64)
+    g = np.minimum(g, E4M3_MAX)
+    # encode the grid value g
+    code = np.zeros(a.shape, np.uint8)
+    sub = g < 2.0 ** -6
+    code[sub] = np.rint(g[sub] / 2.0 ** -9).astype(np.uint8)
+    nrm = ~sub
+    gn = g[nrm]
+    en = np.floor(np.log2(gn))
+    mant = np.rint((gn / np.exp2(en) - 1.0) * 8.0)
+    code[nrm] = ((en + 7).astype(np.int64) << 3 | mant.astype(np.int64)).astype(np.uint8)
+    return code | sign
+
+
+def e4m3_decode(code):
+    """e4m3 codes -> fp32 values (the code 0x7F / 0xFF, NaN, is not produced)."""
+    c = np.asarray(code, np.uint8).astype(np.int64)
+    s = np.where(c & 0x80, -1.0, 1.0)
+    ef = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(ef == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(ef - 7.0))
+    return (s * mag).astype(F32)
+
+
+def quantize_rows_fp8(rows):
+    """One fp32 scale per row (absmax / 448; 1 for an all-zero row) and the
+    row's e4m3 codes of x / scale, both in fp32 arithmetic."""
+    r = np.asarray(rows, F32)
+    amax = np.abs(r).max(axis=-1)
+    scale = np.where(amax > 0, amax / F32(E4M3_MAX), F32(1.0)).astype(F32)
+    return e4m3_encode(r / scale[..., None]), scale
+
+
+def dequantize_rows_fp8(codes, scale):
+    """code value times the row's scale (one fp32 product), rounded to bf16;
+    returned as the fp32 value of that bf16."""
+    import torch
+    v = e4m3_decode(codes) * np.asarray(scale, F32)[..., None]
+    return torch.from_numpy(np.ascontiguousarray(v, F32)).to(torch.bfloat16).float().numpy()
+
+
+def ep_layout_fp8(x, idx, inv, E, n_ep, T):
+    """The expert-parallel layout with an FP8 send buffer: the same slots as
+    ep_layout; slot p carries the codes and scale of its token's row, empty
+    slots carry zero codes and scale 0."""
+    lay = ep_layout(idx, inv, E, n_ep, T)
+    k = np.asarray(idx).reshape(T, -1).shape[1]
+    codes_t, scale_t = quantize_rows_fp8(np.asarray(x, F32))
+    sidx = lay["send_idx"]
+    d = codes_t.shape[1]
+    send = np.zeros((sidx.size, d), np.uint8)
+    sc = np.zeros(sidx.size, F32)
+    ok = sidx >= 0
+    send[ok] = codes_t[sidx[ok] // k]
+    sc[ok] = scale_t[sidx[ok] // k]
+    lay["send_fp8"] = send
+    lay["send_scale"] = sc
+    return lay
