@@ -472,8 +472,8 @@ def eplb_dispatch(idx, inv, offsets, counts, plan, n_ranks, T, capacity=0):
 # wire": FP8 halves s_disp).  The pages fix neither the FP8 format nor the
 # scale granularity: this restatement uses e4m3 (1 sign, 4 exponent bits with
 # bias 7, 3 mantissa bits; largest finite value 448) with one fp32 scale per
-# dispatched row, scale = absmax(row) / 448, code = e4m3(x / scale), rounding
-# to nearest even and saturating at +-448.  Floating-point steps are fp32, as
+# dispatched row, scale = absmax(row) / 448, code = e4m3(x * (448 / absmax)),
+# rounding to nearest even and saturating at +-448.  Floating-point steps are fp32, as
 # on the device, because they decide integer codes.
 # ----------------------------------------------------------------------------
 
@@ -515,12 +515,16 @@ def e4m3_decode(code):
 
 
 def quantize_rows_fp8(rows):
-    """One fp32 scale per row (absmax / 448; 1 for an all-zero row) and the
-    row's e4m3 codes of x / scale, both in fp32 arithmetic."""
+    """One fp32 scale per row, scale = absmax / 448 (1 for an all-zero row),
+    and the row's e4m3 codes of x * (448 / absmax): one fp32 division per row
+    for each of the two factors, one fp32 product per element."""
     r = np.asarray(rows, F32)
     amax = np.abs(r).max(axis=-1)
-    scale = np.where(amax > 0, amax / F32(E4M3_MAX), F32(1.0)).astype(F32)
-    return e4m3_encode(r / scale[..., None]), scale
+    nz = amax > 0
+    safe = np.where(nz, amax, F32(1.0)).astype(F32)
+    scale = np.where(nz, safe / F32(E4M3_MAX), F32(1.0)).astype(F32)
+    inv = np.where(nz, F32(E4M3_MAX) / safe, F32(1.0)).astype(F32)
+    return e4m3_encode((r * inv[..., None]).astype(F32)), scale
 
 
 def dequantize_rows_fp8(codes, scale):
