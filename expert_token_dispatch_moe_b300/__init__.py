@@ -31,7 +31,8 @@ ERRORS = {
 EXPORTS = ("moe_validate_cfg", "moe_grouped_rows", "moe_workspace_bytes", "moe_workspace_init",
            "moe_pack_router", "moe_router_logits", "moe_route", "moe_permute", "moe_permute_noalloc",
            "moe_ep_layout", "moe_pack_w13",
-           "moe_grouped_ffn", "moe_combine", "moe_get_device_status", "moe_strerror",
+           "moe_grouped_ffn", "moe_combine", "moe_bias_update", "moe_eplb_plan",
+           "moe_eplb_dispatch", "moe_get_device_status", "moe_strerror",
            "moe_last_launch_count")
 
 
@@ -84,6 +85,9 @@ _sig = {
     "moe_pack_w13": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
     "moe_grouped_ffn": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
+    "moe_bias_update": (ctypes.c_int, [_CFG, _P, ctypes.c_float, _P, _P]),
+    "moe_eplb_plan": (ctypes.c_int, [_CFG, _P, ctypes.c_int32, _P, _P, _P, _P, _P, _P]),
+    "moe_eplb_dispatch": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_get_device_status": (ctypes.c_int, [_P, _P]),
     "moe_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_last_launch_count": (ctypes.c_int, []),
@@ -194,6 +198,26 @@ def moe_grouped_ffn(cfg, x_sorted, x, counts, offsets, W13, W2, h, y_sorted, ws,
 def moe_combine(cfg, y_sorted, inv, topk_gate, y, stream=None):
     _check(_lib.moe_combine(ctypes.byref(cfg), _ptr(y_sorted), _ptr(inv), _ptr(topk_gate), _ptr(y),
                             _stream(stream)), "moe_combine")
+
+
+def moe_bias_update(cfg, counts, lr, bias, stream=None):
+    _check(_lib.moe_bias_update(ctypes.byref(cfg), _ptr(counts), float(lr), _ptr(bias),
+                                _stream(stream)), "moe_bias_update")
+
+
+def moe_eplb_plan(cfg, loads, slots_per_rank, copies, copy_offset, copy_rank, slot_expert,
+                  rank_load, stream=None):
+    _check(_lib.moe_eplb_plan(ctypes.byref(cfg), _ptr(loads), int(slots_per_rank), _ptr(copies),
+                              _ptr(copy_offset), _ptr(copy_rank), _ptr(slot_expert),
+                              _ptr(rank_load), _stream(stream)), "moe_eplb_plan")
+
+
+def moe_eplb_dispatch(cfg, topk_idx, counts, offsets, inv, copies, copy_offset, copy_rank,
+                      dest_rank, count_mat, stream=None):
+    _check(_lib.moe_eplb_dispatch(ctypes.byref(cfg), _ptr(topk_idx), _ptr(counts), _ptr(offsets),
+                                  _ptr(inv), _ptr(copies), _ptr(copy_offset), _ptr(copy_rank),
+                                  _ptr(dest_rank), _ptr(count_mat), _stream(stream)),
+           "moe_eplb_dispatch")
 
 
 def moe_get_device_status(ws, stream=None) -> int:

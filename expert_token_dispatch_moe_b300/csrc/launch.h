@@ -35,6 +35,16 @@ int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
 int launch_combine(const moe_cfg& c, const void* y_sorted, const int32_t* inv, const float* gate,
                    void* y, cudaStream_t st);
 
+int launch_bias_update(const moe_cfg& c, const int32_t* counts, float lr, float* bias,
+                       cudaStream_t st);
+int launch_eplb_plan(const moe_cfg& c, const int32_t* loads, int slots, int32_t* copies,
+                     int32_t* copy_offset, int32_t* copy_rank, int32_t* slot_expert,
+                     double* rank_load, cudaStream_t st);
+int launch_eplb_dispatch(const moe_cfg& c, const int32_t* idx, const int32_t* inv,
+                         const int32_t* offsets, const int32_t* counts, const int32_t* copies,
+                         const int32_t* copy_offset, const int32_t* copy_rank, int32_t* dest,
+                         int32_t* C, cudaStream_t st);
+
 // Row move shared by the permute and the send-buffer fill: for each token t
 // and slot j, copy x[t] to dst[rows[t*k + j]] when that row is >= 0.
 int launch_row_scatter(const void* x, int T, int d, int k, const int32_t* rows, void* dst,

@@ -231,6 +231,42 @@ MOE_API int moe_combine(const moe_cfg* c, const moe_bf16* y_sorted, const int32_
   return launch_combine(*c, y_sorted, inv, topk_gate, y, static_cast<cudaStream_t>(stream));
 }
 
+MOE_API int moe_bias_update(const moe_cfg* c, const int32_t* counts, float lr, float* bias,
+                            void* stream) {
+  reset_launches();
+  MOE_TRY(moe_validate_cfg(c));
+  MOE_TRY(check_ptrs({counts, bias}));
+  MOE_TRY(device_ok());
+  return launch_bias_update(*c, counts, lr, bias, static_cast<cudaStream_t>(stream));
+}
+
+MOE_API int moe_eplb_plan(const moe_cfg* c, const int32_t* loads, int32_t slots_per_rank,
+                          int32_t* copies, int32_t* copy_offset, int32_t* copy_rank,
+                          int32_t* slot_expert, double* rank_load, void* stream) {
+  reset_launches();
+  MOE_TRY(moe_validate_cfg(c));
+  if (slots_per_rank < 1 || int64_t(c->n_ep) * slots_per_rank < c->E ||
+      int64_t(c->n_ep) * slots_per_rank > 8192)
+    return MOE_E_SHAPE;
+  MOE_TRY(check_ptrs({loads, copies, copy_offset, copy_rank, slot_expert, rank_load}));
+  MOE_TRY(device_ok());
+  return launch_eplb_plan(*c, loads, slots_per_rank, copies, copy_offset, copy_rank, slot_expert,
+                          rank_load, static_cast<cudaStream_t>(stream));
+}
+
+MOE_API int moe_eplb_dispatch(const moe_cfg* c, const int32_t* topk_idx, const int32_t* counts,
+                              const int32_t* offsets, const int32_t* inv, const int32_t* copies,
+                              const int32_t* copy_offset, const int32_t* copy_rank,
+                              int32_t* dest_rank, int32_t* count_mat, void* stream) {
+  reset_launches();
+  MOE_TRY(moe_validate_cfg(c));
+  MOE_TRY(check_ptrs({topk_idx, counts, offsets, inv, copies, copy_offset, copy_rank, dest_rank,
+                      count_mat}));
+  MOE_TRY(device_ok());
+  return launch_eplb_dispatch(*c, topk_idx, inv, offsets, counts, copies, copy_offset, copy_rank,
+                              dest_rank, count_mat, static_cast<cudaStream_t>(stream));
+}
+
 MOE_API int moe_get_device_status(void* ws, void* stream) {
   reset_launches();
   if (!ws) return MOE_E_WORKSPACE;

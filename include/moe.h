@@ -240,6 +240,59 @@ int moe_grouped_ffn(const moe_cfg* cfg, const moe_bf16* x_sorted, const moe_bf16
 int moe_combine(const moe_cfg* cfg, const moe_bf16* y_sorted, const int32_t* inv,
                 const float* topk_gate, moe_bf16* y, void* stream);
 
+/* Load balancing, step 1: the auxiliary-loss-free bias update ("05 - Expert
+ * Parallelism (MoE)", "Load balancing" (b)).  After a step, with the tokens
+ * each expert received:
+ *   bias[e] += lr * (avg_load - counts[e]),  avg_load = sum(counts) / E,
+ * computed in fp64 and rounded once to fp32.  The bias is the selection bias
+ * of moe_route (it changes which experts are chosen, never the gates).
+ *   counts  int32 [E] (moe_permute's counts, or any per-expert load)
+ *   bias    fp32 [E], updated in place
+ * One CTA; asynchronous on `stream`. */
+int moe_bias_update(const moe_cfg* cfg, const int32_t* counts, float lr, float* bias,
+                    void* stream);
+
+/* Load balancing, step 2: redundant experts placed by replicate-then-pack
+ * ("Expert parallelism", "Load imbalance becomes idle time").  The n_ep ranks
+ * have slots_per_rank expert slots each (n_ep * slots_per_rank >= E, at most
+ * 8192 slots in all).
+ *   Replicate: the spare slots go one at a time to the expert with the largest
+ *   load per copy loads[e] / copies[e] (equal ratios: the lower expert).
+ *   Pack: the copies, by load per copy (largest first; equal: lower expert,
+ *   then lower copy), each go to the rank with the smallest load so far among
+ *   those with a free slot (equal loads: the lower rank).
+ * Ratios are compared exactly (64-bit cross products); rank loads are fp64 sums
+ * of loads[e] / copies[e] in placement order.
+ *   loads       int32 [E] >= 0 (for example moe_permute's counts)
+ *   copies      int32 [E] out: copies of each expert (>= 1)
+ *   copy_offset int32 [E] out: exclusive prefix sum of copies
+ *   copy_rank   int32 [n_ep * slots_per_rank] out: entry copy_offset[e] + j is
+ *               the rank holding copy j of expert e (entries past the total
+ *               number of copies are not written)
+ *   slot_expert int32 [n_ep, slots_per_rank] out: expert in each filled slot in
+ *               fill order, -1 in empty slots
+ *   rank_load   fp64 [n_ep] out: planned load of each rank
+ * One CTA; asynchronous on `stream`.  MOE_E_SHAPE when the slots do not fit. */
+int moe_eplb_plan(const moe_cfg* cfg, const int32_t* loads, int32_t slots_per_rank,
+                  int32_t* copies, int32_t* copy_offset, int32_t* copy_rank,
+                  int32_t* slot_expert, double* rank_load, void* stream);
+
+/* Load balancing, step 3: dispatch over the copies of a plan.  Expert e's kept
+ * assignments, in their stable order (rank r = inv[a] - offsets[e] among m
+ * kept), are split evenly over its q copies: copy j takes ranks
+ * [floor(j*m/q), floor((j+1)*m/q)).
+ *   topk_idx, counts, offsets, inv      as written by moe_route / moe_permute
+ *   copies, copy_offset, copy_rank      as written by moe_eplb_plan
+ *   dest_rank  int32 [A] out: rank holding the copy that processes assignment a
+ *              (-1 when dropped)
+ *   count_mat  int32 [n_ep, n_ep] out: C[s][g] = assignments of source rank s
+ *              (tokens [s*T_loc, (s+1)*T_loc)) processed on rank g
+ * Asynchronous on `stream`. */
+int moe_eplb_dispatch(const moe_cfg* cfg, const int32_t* topk_idx, const int32_t* counts,
+                      const int32_t* offsets, const int32_t* inv, const int32_t* copies,
+                      const int32_t* copy_offset, const int32_t* copy_rank, int32_t* dest_rank,
+                      int32_t* count_mat, void* stream);
+
 /* Synchronises `stream`, then returns and clears the workspace status word:
  * MOE_OK, MOE_E_DEVICE_DATA or MOE_E_DEVICE_TIMEOUT (or MOE_E_CUDA). */
 int moe_get_device_status(void* ws, void* stream);
