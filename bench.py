@@ -140,6 +140,59 @@ def _algorithmic(cfg, counts_np):
     return out
 
 
+def _time_extras(m, layer, c, cfg, x, st, flush, counts, pk, reps):
+    """Calls outside the layer step, timed alone with CUDA events (L2 flushed
+    before each): the FP8 dispatch pair and the load-balancing kernels."""
+    dev = x.device
+
+    def timed(fn):
+        out = []
+        for _ in range(reps + 1):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            fn()
+            b.record(st)
+            out.append((a, b))
+        torch.cuda.synchronize(dev)
+        return float(np.mean([a.elapsed_time(b) for a, b in out[1:]]))
+
+    A, d = cfg.A, cfg.d
+    send_fp8 = torch.empty(A, d, dtype=torch.uint8, device=dev)
+    send_scale = torch.empty(A, dtype=torch.float32, device=dev)
+    ms_pack = timed(lambda: m.moe_ep_layout_fp8(c, layer.topk_idx, layer.offsets, layer.inv,
+                                                layer.count_mat, layer.send_off, layer.recv_off,
+                                                layer.send_idx, x, send_fp8, send_scale,
+                                                layer.ws))
+    ms_recv = timed(lambda: m.moe_dispatch_recv_fp8(c, send_fp8, send_scale, layer.send_idx,
+                                                    layer.inv, layer.x_sorted))
+    kept = int(np.minimum(counts, cfg.capacity).sum()) if cfg.capacity else A
+    b_pack = cfg.T * d * 2 + A * d + 4 * A + 16 * A
+    b_recv = A * d + 4 * A + 8 * A + kept * d * 2
+    gbs = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
+    out = {"ep_layout_fp8": {"ms": ms_pack, "gbs": gbs(b_pack, ms_pack),
+                             "frac_hbm": gbs(b_pack, ms_pack) / pk["hbm_gbs"]},
+           "dispatch_recv_fp8": {"ms": ms_recv, "gbs": gbs(b_recv, ms_recv),
+                                 "frac_hbm": gbs(b_recv, ms_recv) / pk["hbm_gbs"]}}
+    del send_fp8
+    bias = torch.zeros(cfg.E, dtype=torch.float32, device=dev)
+    out["bias_update"] = {"ms": timed(lambda: m.moe_bias_update(c, layer.counts, 1e-4, bias))}
+    slots = cfg.E // cfg.n_ep + 1
+    i32 = dict(dtype=torch.int32, device=dev)
+    copies, coff = torch.empty(cfg.E, **i32), torch.empty(cfg.E, **i32)
+    crank = torch.empty(cfg.n_ep * slots, **i32)
+    sexp = torch.empty(cfg.n_ep, slots, **i32)
+    rload = torch.empty(cfg.n_ep, dtype=torch.float64, device=dev)
+    out["eplb_plan"] = {"ms": timed(lambda: m.moe_eplb_plan(c, layer.counts, slots, copies, coff,
+                                                            crank, sexp, rload)),
+                        "slots_per_rank": slots}
+    dest = torch.empty(A, **i32)
+    Cm = torch.empty(cfg.n_ep, cfg.n_ep, **i32)
+    out["eplb_dispatch"] = {"ms": timed(lambda: m.moe_eplb_dispatch(
+        c, layer.topk_idx, layer.counts, layer.offsets, layer.inv, copies, coff, crank, dest, Cm))}
+    return out
+
+
 def _kernel_source_digest():
     """sha1 over the sources of the grouped GEMM (its kernel and PTX wrappers)."""
     import hashlib
@@ -277,6 +330,7 @@ def run_ours(args, cfg):
     counts = layer.counts.cpu().numpy()
     alg = _algorithmic(cfg, counts)
     pk = _peaks()
+    extra = _time_extras(m, layer, c, cfg, x, st, flush, counts, pk, reps=max(3, min(20, args.steps)))
     kt = {n: float(per[:, j].mean()) for j, n in enumerate(names)}  # ms per call
     ffn_tflops = alg["ffn_flops"] / (kt["grouped_ffn"] * 1e-3) / 1e12
     gbs = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
@@ -294,6 +348,7 @@ def run_ours(args, cfg):
         "combine": {"ms": kt["combine"], "gbs": gbs(alg["combine_bytes"], kt["combine"]),
                     "frac_hbm": gbs(alg["combine_bytes"], kt["combine"]) / pk["hbm_gbs"]},
     }
+    kernels.update(extra)
     res = {
         "metric": METRIC,
         "value": cfg.T * world / (step_ms * 1e-3),

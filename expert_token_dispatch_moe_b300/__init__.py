@@ -30,7 +30,7 @@ ERRORS = {
 }
 EXPORTS = ("moe_validate_cfg", "moe_grouped_rows", "moe_workspace_bytes", "moe_workspace_init",
            "moe_pack_router", "moe_router_logits", "moe_route", "moe_permute", "moe_permute_noalloc",
-           "moe_ep_layout", "moe_pack_w13",
+           "moe_ep_layout", "moe_ep_layout_fp8", "moe_dispatch_recv_fp8", "moe_pack_w13",
            "moe_grouped_ffn", "moe_combine", "moe_bias_update", "moe_eplb_plan",
            "moe_eplb_dispatch", "moe_get_device_status", "moe_strerror",
            "moe_last_launch_count")
@@ -82,6 +82,9 @@ _sig = {
     "moe_permute": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute_noalloc": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_ep_layout": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_ep_layout_fp8": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                         _P]),
+    "moe_dispatch_recv_fp8": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
     "moe_pack_w13": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
     "moe_grouped_ffn": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
@@ -181,6 +184,21 @@ def moe_ep_layout(cfg, topk_idx, offsets, inv, count_mat, send_off, recv_off, se
     _check(_lib.moe_ep_layout(ctypes.byref(cfg), _ptr(topk_idx), _ptr(offsets), _ptr(inv),
                               _ptr(count_mat), _ptr(send_off), _ptr(recv_off), _ptr(send_idx),
                               _ptr(x), _ptr(send_buf), p, n, _stream(stream)), "moe_ep_layout")
+
+
+def moe_ep_layout_fp8(cfg, topk_idx, offsets, inv, count_mat, send_off, recv_off, send_idx, x,
+                      send_fp8, send_scale, ws, stream=None):
+    p, n = _ws(ws)
+    _check(_lib.moe_ep_layout_fp8(ctypes.byref(cfg), _ptr(topk_idx), _ptr(offsets), _ptr(inv),
+                                  _ptr(count_mat), _ptr(send_off), _ptr(recv_off),
+                                  _ptr(send_idx), _ptr(x), _ptr(send_fp8), _ptr(send_scale), p, n,
+                                  _stream(stream)), "moe_ep_layout_fp8")
+
+
+def moe_dispatch_recv_fp8(cfg, send_fp8, send_scale, send_idx, inv, x_sorted, stream=None):
+    _check(_lib.moe_dispatch_recv_fp8(ctypes.byref(cfg), _ptr(send_fp8), _ptr(send_scale),
+                                      _ptr(send_idx), _ptr(inv), _ptr(x_sorted), _stream(stream)),
+           "moe_dispatch_recv_fp8")
 
 
 def moe_pack_w13(cfg, W1, W3, W13, stream=None):

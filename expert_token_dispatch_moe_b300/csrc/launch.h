@@ -45,6 +45,11 @@ int launch_eplb_dispatch(const moe_cfg& c, const int32_t* idx, const int32_t* in
                          const int32_t* copy_offset, const int32_t* copy_rank, int32_t* dest,
                          int32_t* C, cudaStream_t st);
 
+int launch_fp8_pack(const moe_cfg& c, const void* x, const int32_t* send_idx, void* send_fp8,
+                    float* send_scale, void* ws, cudaStream_t st);
+int launch_fp8_recv(const moe_cfg& c, const void* send_fp8, const float* send_scale,
+                    const int32_t* send_idx, const int32_t* inv, void* x_sorted, cudaStream_t st);
+
 // Row move shared by the permute and the send-buffer fill: for each token t
 // and slot j, copy x[t] to dst[rows[t*k + j]] when that row is >= 0.
 int launch_row_scatter(const void* x, int T, int d, int k, const int32_t* rows, void* dst,

@@ -195,6 +195,35 @@ MOE_API int moe_ep_layout(const moe_cfg* c, const int32_t* topk_idx, const int32
                           send_buf, ws, static_cast<cudaStream_t>(stream));
 }
 
+MOE_API int moe_ep_layout_fp8(const moe_cfg* c, const int32_t* topk_idx, const int32_t* offsets,
+                              const int32_t* inv, int32_t* count_mat, int32_t* send_off,
+                              int32_t* recv_off, int32_t* send_idx, const moe_bf16* x,
+                              uint8_t* send_fp8, float* send_scale, void* ws, size_t ws_bytes,
+                              void* stream) {
+  reset_launches();
+  MOE_TRY(moe_validate_cfg(c));
+  MOE_TRY(check_ptrs({topk_idx, offsets, inv, count_mat, send_off, recv_off, send_idx, x,
+                      send_fp8, send_scale}));
+  if (c->n_ep > 1024) return MOE_E_SHAPE;
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  MOE_TRY(device_ok());
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_TRY(launch_ep_layout(*c, topk_idx, offsets, inv, count_mat, send_off, recv_off, send_idx,
+                           nullptr, nullptr, ws, st));
+  return launch_fp8_pack(*c, x, send_idx, send_fp8, send_scale, ws, st);
+}
+
+MOE_API int moe_dispatch_recv_fp8(const moe_cfg* c, const uint8_t* send_fp8,
+                                  const float* send_scale, const int32_t* send_idx,
+                                  const int32_t* inv, moe_bf16* x_sorted, void* stream) {
+  reset_launches();
+  MOE_TRY(moe_validate_cfg(c));
+  MOE_TRY(check_ptrs({send_fp8, send_scale, send_idx, inv, x_sorted}));
+  MOE_TRY(device_ok());
+  return launch_fp8_recv(*c, send_fp8, send_scale, send_idx, inv, x_sorted,
+                         static_cast<cudaStream_t>(stream));
+}
+
 MOE_API int moe_pack_w13(const moe_cfg* c, const moe_bf16* W1, const moe_bf16* W3, moe_bf16* W13,
                          void* stream) {
   reset_launches();

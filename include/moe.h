@@ -174,6 +174,35 @@ int moe_ep_layout(const moe_cfg* cfg, const int32_t* topk_idx, const int32_t* of
                   int32_t* recv_off, int32_t* send_idx, const moe_bf16* x,
                   moe_bf16* send_buf, void* ws, size_t ws_bytes, void* stream);
 
+/* Steps 2-4 with an FP8 send buffer ("Expert parallelism", "A worked example at
+ * DeepSeek-V3's shape": dispatch in FP8, s = 1 byte, combine in BF16; "Lower
+ * precision on the wire").  The same count matrix, offsets and slots as
+ * moe_ep_layout; the send buffer holds e4m3 codes with one fp32 scale per row:
+ *   scale = absmax(x[t]) / 448 (1 for an all-zero row),
+ *   code  = e4m3(x * (448 / absmax)), rounded to nearest even, saturated at 448.
+ * The format and the per-row granularity are this library's reading (the
+ * description fixes only the byte width).
+ *   send_fp8   uint8 [A, d] out: codes of slot p's token row; zero in empty slots
+ *   send_scale fp32 [A] out: the row's scale; 0 in empty slots
+ *   other arguments as for moe_ep_layout (x is required). */
+int moe_ep_layout_fp8(const moe_cfg* cfg, const int32_t* topk_idx, const int32_t* offsets,
+                      const int32_t* inv, int32_t* count_mat, int32_t* send_off,
+                      int32_t* recv_off, int32_t* send_idx, const moe_bf16* x,
+                      uint8_t* send_fp8, float* send_scale, void* ws, size_t ws_bytes,
+                      void* stream);
+
+/* The receiving side of an FP8 dispatch: slot p carries assignment
+ * a = send_idx[p] (skipped when -1), whose row in the expert-grouped buffer
+ * is inv[a]; x_sorted[inv[a]] = bf16(code * scale) element by element (one
+ * fp32 product, rounded to nearest even).  Rows no slot maps to (capacity
+ * padding) are not written.
+ *   send_fp8, send_scale, send_idx  from moe_ep_layout_fp8
+ *   inv                              from moe_permute
+ *   x_sorted   bf16 [R, d] out */
+int moe_dispatch_recv_fp8(const moe_cfg* cfg, const uint8_t* send_fp8, const float* send_scale,
+                          const int32_t* send_idx, const int32_t* inv, moe_bf16* x_sorted,
+                          void* stream);
+
 /* moe_permute without a workspace argument, for callers that cannot allocate
  * device memory.  The pages have no counterpart to this entry point; it exists
  * for integration.  Some callers are handed only their input and output tensors
