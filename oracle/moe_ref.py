@@ -21,7 +21,7 @@ __all__ = [
     "imbalance_eta", "alltoall_bytes", "dispatch_combine_bytes_per_token",
     "bias_update", "eplb_replicate", "eplb_pack", "eplb_plan", "eplb_dispatch",
     "E4M3_MAX", "e4m3_encode", "e4m3_decode", "quantize_rows_fp8", "dequantize_rows_fp8",
-    "ep_layout_fp8",
+    "ep_layout_fp8", "swiglu_expert_backward", "moe_backward",
 ]
 
 F64 = np.float64
@@ -552,3 +552,68 @@ def ep_layout_fp8(x, idx, inv, E, n_ep, T):
     lay["send_fp8"] = send
     lay["send_scale"] = sc
     return lay
+
+
+# ----------------------------------------------------------------------------
+# Backward ([EP] "Expert parallelism": the dispatch and combine run "twice
+# more in the backward pass"): the gradients of the layer with the routing
+# decision held fixed.  Step 7 backward is a dispatch of dy (each kept
+# assignment receives gate * dy of its token, and its gate receives <dy, o>);
+# step 5 backward runs the experts' transposed products; step 2 backward is a
+# combine (each token sums the input gradients of its kept rows).
+# ----------------------------------------------------------------------------
+
+def swiglu_expert_backward(X, W1, W3, W2, dO):
+    """Gradients of O = W2 (silu(W1 x) * (W3 x)) for rows X given dO (fp64):
+    returns (dX, dW1, dW3, dW2) with silu'(u) = s (1 + u (1 - s)), s = 1/(1+e^-u)."""
+    X = np.asarray(X, F64)
+    W1 = np.asarray(W1, F64)
+    W3 = np.asarray(W3, F64)
+    W2 = np.asarray(W2, F64)
+    dO = np.asarray(dO, F64)
+    u = X @ W1.T
+    v = X @ W3.T
+    s = 1.0 / (1.0 + np.exp(-u))
+    h = u * s * v
+    dh = dO @ W2
+    du = dh * v * s * (1.0 + u * (1.0 - s))
+    dv = dh * u * s
+    return du @ W1 + dv @ W3, du.T @ X, dv.T @ X, dO.T @ h
+
+
+def moe_backward(x, scores, cfg, W1, W3, W2, dy, bias=None):
+    """Backward of moe_forward for output gradient dy [T, d] (fp64), routing
+    (indices and kept rows) fixed: returns dict with dx [T, d], dW1/dW3
+    [E(+1), f, d], dW2 [E(+1), d, f] and dgate [T, k] (the gradient with
+    respect to the gate values; dropped assignments get 0)."""
+    T, E, k = cfg.T, cfg.E, cfg.k
+    x = np.asarray(x, F64)
+    dy = np.asarray(dy, F64)
+    idx = select_experts(scores, k, bias, cfg.n_groups, cfg.topk_groups)
+    gates = gate_weights(scores, idx, cfg.score_fn, cfg.norm_topk).reshape(-1)
+    perm = permute(idx, E, cfg.capacity)
+    n = E + (1 if cfg.has_shared else 0)
+    f, d = np.asarray(W1[0]).shape
+    dx = np.zeros((T, d), F64)
+    dW1 = np.zeros((n, f, d), F64)
+    dW3 = np.zeros((n, f, d), F64)
+    dW2 = np.zeros((n, d, f), F64)
+    dgate = np.zeros(T * k, F64)
+    order, offsets, kept = perm["order"], perm["offsets"], perm["kept"]
+    for e in range(E):
+        rows = np.arange(int(offsets[e]), int(offsets[e]) + int(kept[e]))
+        if rows.size == 0:
+            continue
+        a = order[rows]
+        t = a // k
+        Xe = x[t]
+        o = swiglu_expert(Xe, W1[e], W3[e], W2[e])
+        dgate[a] = (dy[t] * o).sum(axis=1)
+        dO = gates[a][:, None] * dy[t]
+        dXe, dW1[e], dW3[e], dW2[e] = swiglu_expert_backward(Xe, W1[e], W3[e], W2[e], dO)
+        np.add.at(dx, t, dXe)
+    if cfg.has_shared:
+        dXs, dW1[E], dW3[E], dW2[E] = swiglu_expert_backward(x, W1[E], W3[E], W2[E], dy)
+        dx += dXs
+    return {"dx": dx, "dW1": dW1, "dW3": dW3, "dW2": dW2, "dgate": dgate.reshape(T, k),
+            "idx": idx, "gates": gates.reshape(T, k), "perm": perm}
