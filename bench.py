@@ -121,8 +121,9 @@ class _Clocks:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def _algorithmic(cfg, counts_np):
-    """Algorithmic FLOPs and bytes of one step (what the method must do)."""
+def _algorithmic(cfg, counts_np, gather=False):
+    """Algorithmic FLOPs and bytes of one step (what the method must do).  With
+    the gather path the permute moves no rows (GEMM 1 reads the token rows)."""
     kept = int(np.minimum(counts_np, cfg.capacity).sum()) if cfg.capacity else cfg.A
     rows_ffn = kept + (cfg.T if cfg.has_shared else 0)
     R = cfg.R
@@ -131,7 +132,8 @@ def _algorithmic(cfg, counts_np):
         "ffn_flops": 6.0 * cfg.d * cfg.f * rows_ffn,
         "router_bytes": cfg.T * cfg.d * b2 + cfg.d * cfg.E * 4 + cfg.T * cfg.E * 4,
         "route_bytes": cfg.T * cfg.E * 4 + cfg.A * 8,
-        "permute_bytes": cfg.T * cfg.d * b2 + R * cfg.d * b2 + 4 * (2 * cfg.A + R + 2 * cfg.E),
+        "permute_bytes": (0 if gather else cfg.T * cfg.d * b2 + R * cfg.d * b2)
+                         + 4 * (2 * cfg.A + R + 2 * cfg.E),
         "layout_bytes": cfg.T * cfg.d * b2 + cfg.A * cfg.d * b2 + 4 * 4 * cfg.A,
         "combine_bytes": (kept + (cfg.T if cfg.has_shared else 0)) * cfg.d * b2
                          + cfg.T * cfg.d * b2 + 8 * cfg.A,
@@ -245,7 +247,8 @@ def run_ours(args, cfg):
     x = synth.make_x(cfg, device=dev, seed=synth.DATA_SEED + rank)
     W_r, lbias = synth.make_router(cfg, device=dev)
     W1, W3, W2 = synth.make_expert_weights(cfg, device=dev)
-    layer = m.MoELayer(cfg, W1, W3, W2, W_r=W_r, logit_bias=lbias, device=dev)
+    gather = args.path == "gather"
+    layer = m.MoELayer(cfg, W1, W3, W2, W_r=W_r, logit_bias=lbias, device=dev, gather=gather)
     del W1, W3
     torch.cuda.empty_cache()
     c = layer.cfg
@@ -261,14 +264,19 @@ def run_ours(args, cfg):
         ev[1].record(st)
         m.moe_route(c, layer.scores, None, layer.topk_idx, layer.topk_gate)
         ev[2].record(st)
-        m.moe_permute(c, x, layer.topk_idx, layer.counts, layer.offsets, layer.order, layer.inv,
-                      layer.x_sorted, layer.ws)
+        m.moe_permute(c, None if gather else x, layer.topk_idx, layer.counts, layer.offsets,
+                      layer.order, layer.inv, None if gather else layer.x_sorted, layer.ws)
         ev[3].record(st)
         m.moe_ep_layout(c, layer.topk_idx, layer.offsets, layer.inv, layer.count_mat,
                         layer.send_off, layer.recv_off, layer.send_idx, x, layer.send_buf, layer.ws)
         ev[4].record(st)
-        m.moe_grouped_ffn(c, layer.x_sorted, x if c.has_shared else None, layer.counts,
-                          layer.offsets, layer.W13, layer.W2, layer.h, layer.y_sorted, layer.ws)
+        if gather:
+            m.moe_grouped_ffn_gather(c, x, layer.order, layer.counts, layer.offsets, layer.W13,
+                                     layer.W2, layer.h, layer.y_sorted, layer.ws)
+        else:
+            m.moe_grouped_ffn(c, layer.x_sorted, x if c.has_shared else None, layer.counts,
+                              layer.offsets, layer.W13, layer.W2, layer.h, layer.y_sorted,
+                              layer.ws)
         ev[5].record(st)
         m.moe_combine(c, layer.y_sorted, layer.inv, layer.topk_gate, layer.y)
         ev[6].record(st)
@@ -328,7 +336,7 @@ def run_ours(args, cfg):
     e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in e_evs]))
 
     counts = layer.counts.cpu().numpy()
-    alg = _algorithmic(cfg, counts)
+    alg = _algorithmic(cfg, counts, gather)
     pk = _peaks()
     extra = _time_extras(m, layer, c, cfg, x, st, flush, counts, pk, reps=max(3, min(20, args.steps)))
     kt = {n: float(per[:, j].mean()) for j, n in enumerate(names)}  # ms per call
@@ -362,7 +370,7 @@ def run_ours(args, cfg):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded: x~N(0,1), expert weights~N(0,1/d), W_r~N(0,1/d) fp32)",
-        "config": {"workload": _workload(cfg), "tokens_per_gpu": cfg.T,
+        "config": {"workload": _workload(cfg), "tokens_per_gpu": cfg.T, "path": args.path,
                    "l2": "flushed between timed steps (512 MiB write, outside the timed events)",
                    "parallelism": f"{world} independent replica(s)"},
         "e2e": {"value": cfg.T * world / (e2e_ms * 1e-3), "unit": "tokens/s",
@@ -492,6 +500,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", default="rows", choices=["rows", "gather"],
+                    help="rows: the permute writes x_sorted and GEMM 1 reads it; gather: the "
+                         "permute computes indices only and GEMM 1 gathers token rows itself")
     ap.add_argument("--override", default="",
                     help="comma-separated field=value changes to the workload, e.g. "
                          "T=1024,E=32,n_ep=8 (a reduced case of the same shape for profiling)")

@@ -31,8 +31,10 @@ ERRORS = {
 EXPORTS = ("moe_validate_cfg", "moe_grouped_rows", "moe_workspace_bytes", "moe_workspace_init",
            "moe_pack_router", "moe_router_logits", "moe_route", "moe_permute", "moe_permute_noalloc",
            "moe_ep_layout", "moe_ep_layout_fp8", "moe_dispatch_recv_fp8", "moe_pack_w13",
-           "moe_grouped_ffn", "moe_combine", "moe_bias_update", "moe_eplb_plan",
-           "moe_eplb_dispatch", "moe_get_device_status", "moe_strerror",
+           "moe_grouped_ffn", "moe_grouped_ffn_gather", "moe_combine", "moe_bias_update", "moe_eplb_plan",
+           "moe_eplb_dispatch", "moe_pack_backward", "moe_combine_backward",
+           "moe_backward_workspace_bytes", "moe_grouped_ffn_backward", "moe_permute_backward",
+           "moe_get_device_status", "moe_strerror",
            "moe_last_launch_count")
 
 
@@ -87,10 +89,18 @@ _sig = {
     "moe_dispatch_recv_fp8": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
     "moe_pack_w13": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
     "moe_grouped_ffn": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_grouped_ffn_gather": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                              _P]),
     "moe_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
     "moe_bias_update": (ctypes.c_int, [_CFG, _P, ctypes.c_float, _P, _P]),
     "moe_eplb_plan": (ctypes.c_int, [_CFG, _P, ctypes.c_int32, _P, _P, _P, _P, _P, _P]),
     "moe_eplb_dispatch": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_pack_backward": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
+    "moe_combine_backward": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_backward_workspace_bytes": (_SZ, [_CFG]),
+    "moe_grouped_ffn_backward": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                                _P, _P, _P, _SZ, _P, _SZ, _P]),
+    "moe_permute_backward": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
     "moe_get_device_status": (ctypes.c_int, [_P, _P]),
     "moe_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_last_launch_count": (ctypes.c_int, []),
@@ -213,6 +223,14 @@ def moe_grouped_ffn(cfg, x_sorted, x, counts, offsets, W13, W2, h, y_sorted, ws,
                                 _stream(stream)), "moe_grouped_ffn")
 
 
+def moe_grouped_ffn_gather(cfg, x, order, counts, offsets, W13, W2, h, y_sorted, ws, stream=None):
+    p, n = _ws(ws)
+    _check(_lib.moe_grouped_ffn_gather(ctypes.byref(cfg), _ptr(x), _ptr(order), _ptr(counts),
+                                       _ptr(offsets), _ptr(W13), _ptr(W2), _ptr(h),
+                                       _ptr(y_sorted), p, n, _stream(stream)),
+           "moe_grouped_ffn_gather")
+
+
 def moe_combine(cfg, y_sorted, inv, topk_gate, y, stream=None):
     _check(_lib.moe_combine(ctypes.byref(cfg), _ptr(y_sorted), _ptr(inv), _ptr(topk_gate), _ptr(y),
                             _stream(stream)), "moe_combine")
@@ -236,6 +254,37 @@ def moe_eplb_dispatch(cfg, topk_idx, counts, offsets, inv, copies, copy_offset, 
                                   _ptr(inv), _ptr(copies), _ptr(copy_offset), _ptr(copy_rank),
                                   _ptr(dest_rank), _ptr(count_mat), _stream(stream)),
            "moe_eplb_dispatch")
+
+
+def moe_pack_backward(cfg, W13, W2, W13t, W2t, stream=None):
+    _check(_lib.moe_pack_backward(ctypes.byref(cfg), _ptr(W13), _ptr(W2), _ptr(W13t), _ptr(W2t),
+                                  _stream(stream)), "moe_pack_backward")
+
+
+def moe_combine_backward(cfg, dy, y_sorted, inv, topk_gate, d_o, dgate, stream=None):
+    _check(_lib.moe_combine_backward(ctypes.byref(cfg), _ptr(dy), _ptr(y_sorted), _ptr(inv),
+                                     _ptr(topk_gate), _ptr(d_o), _ptr(dgate), _stream(stream)),
+           "moe_combine_backward")
+
+
+def moe_backward_workspace_bytes(cfg) -> int:
+    return _lib.moe_backward_workspace_bytes(ctypes.byref(cfg))
+
+
+def moe_grouped_ffn_backward(cfg, x_sorted, x, counts, offsets, W13, W13t, W2t, h, d_o, dx_sorted,
+                             dW13, dW2, bws, ws, stream=None):
+    bp, bn = _ws(bws)
+    p, n = _ws(ws)
+    _check(_lib.moe_grouped_ffn_backward(ctypes.byref(cfg), _ptr(x_sorted), _ptr(x),
+                                         _ptr(counts), _ptr(offsets), _ptr(W13), _ptr(W13t),
+                                         _ptr(W2t), _ptr(h), _ptr(d_o), _ptr(dx_sorted),
+                                         _ptr(dW13), _ptr(dW2), bp, bn, p, n, _stream(stream)),
+           "moe_grouped_ffn_backward")
+
+
+def moe_permute_backward(cfg, dx_sorted, inv, dx, stream=None):
+    _check(_lib.moe_permute_backward(ctypes.byref(cfg), _ptr(dx_sorted), _ptr(inv), _ptr(dx),
+                                     _stream(stream)), "moe_permute_backward")
 
 
 def moe_get_device_status(ws, stream=None) -> int:

@@ -33,7 +33,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
   const int my_row = (lane < k) ? __ldg(inv + size_t(t) * k + lane) : -1;
-  const float my_g = (lane < k) ? __ldg(gate + size_t(t) * k + lane) : 0.0f;
+  // gate == nullptr: unit gates (the permute's backward sums the rows)
+  const float my_g = (lane < k) ? (gate ? __ldg(gate + size_t(t) * k + lane) : 1.0f) : 0.0f;
   const uint4* shared_row = y_sorted + size_t(R + t) * vec;
   if (KT > 0) {
     int rows[KT > 0 ? KT : 1];

@@ -44,6 +44,12 @@ inline WsLayout ws_layout(const moe_cfg& c) {
   return L;
 }
 
+// Workspace of the layer's backward (moe_backward_workspace_bytes).
+struct BwdLayout {
+  size_t g1, dg1, kpad, tr, total;
+  size_t kub;  // columns of the transposed operands (upper bound on the padded rows)
+};
+
 template <typename T>
 inline T* ws_ptr(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
@@ -137,6 +143,21 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// Four rows r0..r3 (any order, any rows of the tensor) of a tensor map whose
+// box is one row high, columns [c0, c0 + box width), into consecutive rows of
+// shared memory at smem_dst (128-byte aligned; the swizzle pattern follows the
+// address, so four such copies at 512-byte steps fill a 1024-byte atom exactly
+// as one 8-row box copy would).
+__device__ __forceinline__ void tma_gather4_2d(void* smem_dst, const CUtensorMap* m, int c0, int r0,
+                                               int r1, int r2, int r3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "r"(smem_u32(bar))
       : "memory");
 }
 

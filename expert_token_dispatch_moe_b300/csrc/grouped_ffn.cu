@@ -44,7 +44,7 @@ constexpr uint64_t DRAIN_NS = 100000000ull;
 constexpr size_t DYN_SMEM = size_t(STAGES) * STAGE_BYTES + 1024;
 }  // namespace gg
 
-enum { kEpiSwiglu = 0, kEpiBf16 = 1, kEpiF32 = 2 };
+enum { kEpiSwiglu = 0, kEpiBf16 = 1, kEpiF32 = 2, kEpiSwigluBwd = 3 };
 
 struct GroupedParams {
   const int32_t* counts;  // nullptr: one dense segment of dense_rows rows at row 0
@@ -58,6 +58,10 @@ struct GroupedParams {
   int mode;               // kEpiSwiglu: out[:, j] = silu(acc[:, gate j]) * acc[:, up j]
                           // kEpiBf16:   out = bf16(acc)
                           // kEpiF32:    out_f32 = acc + col_bias (sigmoid if set), fp32
+                          // kEpiSwigluBwd: acc = dh (columns j of the expert width);
+                          //   with u, v = aux[:, gate j], aux[:, up j] (packed like W13)
+                          //   and s = sigmoid(u): out[:, gate j] = dh v s (1 + u (1 - s)),
+                          //   out[:, up j] = dh u s
   int shared_a_separate;  // 1: shared expert's A rows come from tmA_sh from row 0
   __nv_bfloat16* out;
   float* out_f32;
@@ -65,6 +69,16 @@ struct GroupedParams {
   int sigmoid;
   int ld_out;
   int* status;
+  const int32_t* gather_order;  // non-null: a routed segment's A rows are gathered from the
+  int gather_k;                 //   token rows, row r -> token gather_order[r] / gather_k
+  const __nv_bfloat16* aux;     // kEpiSwigluBwd: the recomputed GEMM 1 output (u | v packed)
+  int ld_aux;
+  // Weight-gradient mode (kpad_off non-null): every segment g is an m_out x N
+  // output block at rows g*m_out, reduced over columns [kpad_off[g],
+  // kpad_off[g+1]) of the transposed operands (A [m_out, K_all], B [N, K_all],
+  // shared by all segments; zero-padded to multiples of 64 per segment).
+  const int32_t* kpad_off;
+  int m_out;
 };
 
 struct GroupedCtl {
@@ -81,7 +95,11 @@ struct GroupedCtl {
 
 __device__ __forceinline__ void segment(const GroupedParams& p, int g, int& rows, int& a_row0,
                                         int& out_row0) {
-  if (p.counts == nullptr) {
+  if (p.kpad_off != nullptr) {
+    rows = p.m_out;
+    a_row0 = 0;
+    out_row0 = g * p.m_out;
+  } else if (p.counts == nullptr) {
     rows = p.dense_rows;
     a_row0 = 0;
     out_row0 = 0;
@@ -130,8 +148,19 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_seg = p.counts ? p.E + p.has_shared : 1;
   const int n_blocks_n = (p.N + BN - 1) / BN;
-  const int kb_per_pass = p.K / BK;
-  const int num_kb = kb_per_pass * p.k_passes;
+  const bool wgrad = p.kpad_off != nullptr;
+  const int kb_per_pass = wgrad ? (1 << 30) : p.K / BK;
+  const int num_kb = wgrad ? 0 : kb_per_pass * p.k_passes;
+  // first column and k-blocks of segment g's reduction
+  auto tile_k = [&](int g, int& k0, int& nkb) {
+    if (wgrad) {
+      k0 = __ldg(p.kpad_off + g);
+      nkb = (__ldg(p.kpad_off + g + 1) - k0) / BK;
+    } else {
+      k0 = 0;
+      nkb = num_kb;
+    }
+  };
 
   // ---- device-side tile schedule: exclusive prefix of tiles per segment ----
   {
@@ -215,34 +244,89 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
   auto is_half = [&](int rows, int m_blk) { return rows - m_blk * BM <= BM / 2; };
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer ----------------
-      uint32_t stage = 0, phase = 0;
-      uint32_t issued = 0, last_phase = 0;  // per-stage bit masks
-      bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+    // ---------------- TMA producer ----------------
+    // Lane 0 waits for free stages and issues the box copies.  With gathered
+    // A rows (p.gather_order) the whole warp takes part: lane j copies rows
+    // 4j..4j+3 of the tile with one four-row gather per k-block.
+    uint32_t stage = 0, phase = 0;
+    uint32_t issued = 0, last_phase = 0;  // per-stage bit masks (lane 0)
+    bool ok = true;
+    if (p.gather_order == nullptr) {
+      if (lane == 0) {
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+          int g, m_blk, n_blk, rows, a_row0, out_row0;
+          decode(t, g, m_blk, n_blk, rows, a_row0, out_row0);
+          const bool sep = p.counts && g >= p.E && p.shared_a_separate;
+          const bool half = is_half(rows, m_blk);
+          const CUtensorMap* ma = half ? (sep ? &tmA_sh64 : &tmA64) : (sep ? &tmA_sh : &tmA);
+          const uint32_t tx = half ? A_BYTES / 2 + B_BYTES : STAGE_BYTES;
+          const int a_row = a_row0 + m_blk * BM;
+          const int b_row = (wgrad ? 0 : g * p.N) + n_blk * BN;
+          int k0, nkb;
+          tile_k(g, k0, nkb);
+          for (int kb = 0; kb < nkb; ++kb) {
+            if (!wait_or_abort(&ctl.empty[stage], phase ^ 1u, ctl, p.status)) { ok = false; break; }
+            uint8_t* sa = smem + stage * STAGE_BYTES;
+            const int pass = kb / kb_per_pass;
+            const int ka = k0 + (kb - pass * kb_per_pass) * BK;
+            mbar_arrive_expect_tx(&ctl.full[stage], tx);
+            tma_load_2d(sa, ma, ka, a_row, &ctl.full[stage]);
+            tma_load_2d(sa + A_BYTES, &tmB, ka, b_row + pass * p.b_pass_rows, &ctl.full[stage]);
+            issued |= 1u << stage;
+            last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+        }
+      }
+    } else {
+      for (int t = blockIdx.x; t < total; t += gridDim.x) {
         int g, m_blk, n_blk, rows, a_row0, out_row0;
         decode(t, g, m_blk, n_blk, rows, a_row0, out_row0);
         const bool sep = p.counts && g >= p.E && p.shared_a_separate;
+        const bool gather = p.gather_order != nullptr && p.counts && g < p.E;
         const bool half = is_half(rows, m_blk);
+        const int n_rows = half ? BM / 2 : BM;
+        int tok[4] = {0, 0, 0, 0};
+        if (gather && 4 * lane < n_rows) {
+          // tokens of rows 4*lane .. 4*lane+3; rows past the segment repeat its first row
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = m_blk * BM + 4 * lane + i;
+            const int src = a_row0 + (r < rows ? r : m_blk * BM);
+            tok[i] = __ldg(p.gather_order + src) / p.gather_k;
+          }
+        }
         const CUtensorMap* ma = half ? (sep ? &tmA_sh64 : &tmA64) : (sep ? &tmA_sh : &tmA);
         const uint32_t tx = half ? A_BYTES / 2 + B_BYTES : STAGE_BYTES;
         const int a_row = a_row0 + m_blk * BM;
         const int b_row = g * p.N + n_blk * BN;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!wait_or_abort(&ctl.empty[stage], phase ^ 1u, ctl, p.status)) { ok = false; break; }
+          if (lane == 0) ok = wait_or_abort(&ctl.empty[stage], phase ^ 1u, ctl, p.status);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
           uint8_t* sa = smem + stage * STAGE_BYTES;
-          uint8_t* sb = sa + A_BYTES;
           const int pass = kb / kb_per_pass;
           const int ka = (kb - pass * kb_per_pass) * BK;
-          mbar_arrive_expect_tx(&ctl.full[stage], tx);
-          tma_load_2d(sa, ma, ka, a_row, &ctl.full[stage]);
-          tma_load_2d(sb, &tmB, ka, b_row + pass * p.b_pass_rows, &ctl.full[stage]);
-          issued |= 1u << stage;
-          last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+          if (lane == 0) mbar_arrive_expect_tx(&ctl.full[stage], tx);
+          __syncwarp();
+          if (gather) {
+            if (4 * lane < n_rows)
+              tma_gather4_2d(sa + lane * 4 * (BK * 2), &tmA, ka, tok[0], tok[1], tok[2], tok[3],
+                             &ctl.full[stage]);
+          } else if (lane == 0) {
+            tma_load_2d(sa, ma, ka, a_row, &ctl.full[stage]);
+          }
+          if (lane == 0) {
+            tma_load_2d(sa + A_BYTES, &tmB, ka, b_row + pass * p.b_pass_rows, &ctl.full[stage]);
+            issued |= 1u << stage;
+            last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+          }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
+        if (!ok) break;
       }
+    }
+    if (lane == 0) {
       if (ok && !ctl.abort) {
         // every stage released by the MMA warp: all its commits have landed
         for (int i = 0; i < STAGES; ++i) {
@@ -266,10 +350,12 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
         decode(t, g, m_blk, n_blk, rows, a_row0, out_row0);
         const uint32_t idesc = is_half(rows, m_blk) ? idesc_bf16_f32(BM / 2, BN)
                                                     : idesc_bf16_f32(BM, BN);
+        int k0, nkb;
+        tile_k(g, k0, nkb);
         if (!wait_or_abort(&ctl.acc_empty[acc], acc_phase ^ 1u, ctl, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = 0; kb < nkb; ++kb) {
           if (!wait_or_abort(&ctl.full[stage], phase, ctl, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint8_t* sa = smem + stage * STAGE_BYTES;
@@ -308,7 +394,56 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
       const bool valid = (!half || lane < 16) && r < rows;
       const size_t orow_idx = size_t(out_row0 + (valid ? r : 0)) * p.ld_out;
       __nv_bfloat16* orow = p.out + orow_idx;
-      if (p.mode == kEpiF32) {
+      int k0, nkb;
+      tile_k(g, k0, nkb);
+      if (nkb == 0) {
+        // an empty reduction (a weight-gradient segment with no rows): zeros
+        const int col0 = n_blk * BN;
+        if (valid)
+          for (int c = 0; c < BN && col0 + c < p.N; c += 8)
+            *reinterpret_cast<uint4*>(orow + col0 + c) = make_uint4(0, 0, 0, 0);
+      } else if (p.mode == kEpiSwigluBwd) {
+        // accumulator columns are expert-width columns j = n_blk*BN + c; u and v
+        // of column j sit at packed columns 256*(j/128) + j%128 and that + 128
+        const __nv_bfloat16* arow = p.aux + size_t(out_row0 + (valid ? r : 0)) * p.ld_aux;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t dv32[32];
+          tmem_ld32(taddr + c, dv32);
+          tmem_ld_wait();
+          const int j = n_blk * BN + c;
+          if (valid && j < p.N) {
+            const int pu = 256 * (j / 128) + (j % 128);
+            const uint4* up = reinterpret_cast<const uint4*>(arow + pu);
+            const uint4* vp = reinterpret_cast<const uint4*>(arow + pu + 128);
+            uint4* dup = reinterpret_cast<uint4*>(orow + pu);
+            uint4* dvp = reinterpret_cast<uint4*>(orow + pu + 128);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint4 uq = __ldg(up + q), vq = __ldg(vp + q);
+              const uint32_t uw[4] = {uq.x, uq.y, uq.z, uq.w}, vw[4] = {vq.x, vq.y, vq.z, vq.w};
+              uint32_t du_out[4], dv_out[4];
+#pragma unroll
+              for (int w = 0; w < 4; ++w) {
+                float du2[2], dvv2[2];
+#pragma unroll
+                for (int hlf = 0; hlf < 2; ++hlf) {
+                  const float u = hlf ? bf16hi(uw[w]) : bf16lo(uw[w]);
+                  const float v = hlf ? bf16hi(vw[w]) : bf16lo(vw[w]);
+                  const float dh = __uint_as_float(dv32[8 * q + 2 * w + hlf]);
+                  const float sg = 1.0f / (1.0f + __expf(-u));
+                  du2[hlf] = dh * v * sg * (1.0f + u * (1.0f - sg));
+                  dvv2[hlf] = dh * u * sg;
+                }
+                du_out[w] = pack_bf16x2(du2[0], du2[1]);
+                dv_out[w] = pack_bf16x2(dvv2[0], dvv2[1]);
+              }
+              dup[q] = make_uint4(du_out[0], du_out[1], du_out[2], du_out[3]);
+              dvp[q] = make_uint4(dv_out[0], dv_out[1], dv_out[2], dv_out[3]);
+            }
+          }
+        }
+      } else if (p.mode == kEpiF32) {
         const int col0 = n_blk * BN;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
@@ -447,6 +582,25 @@ static int set_smem_attr() {
   return err == cudaSuccess ? MOE_OK : MOE_E_CUDA;
 }
 
+#define MOE_TRY_INTERNAL(expr)      \
+  do {                              \
+    const int _rc = (expr);         \
+    if (_rc != MOE_OK) return _rc;  \
+  } while (0)
+
+// One grouped GEMM on at most one CTA per SM and no more CTAs than an upper
+// bound on its tiles (rows_ub rows over at most n_seg segments).
+static int launch_gg(int64_t rows_ub, int n_seg, const CUtensorMap& a, const CUtensorMap& a_sh,
+                     const CUtensorMap& a64, const CUtensorMap& a_sh64, const CUtensorMap& b,
+                     const GroupedParams& p, cudaStream_t st) {
+  const int sms = device_sm_count();
+  const long long tiles = (rows_ub / gg::BM + n_seg) * ((p.N + gg::BN - 1) / gg::BN);
+  const int grid = int(tiles < sms ? tiles : sms);
+  grouped_gemm_kernel<<<grid, gg::THREADS, gg::DYN_SMEM, st>>>(a, a_sh, a64, a_sh64, b, p);
+  note_launches(1);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_E_CUDA;
+}
+
 static int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -529,8 +683,9 @@ int launch_pack_router(const moe_cfg& c, const float* W, void* out, cudaStream_t
 }
 
 int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
-                       const int32_t* counts, const int32_t* offsets, const void* W13,
-                       const void* W2, void* h, void* y_sorted, void* ws, cudaStream_t st) {
+                       const int32_t* gather_order, const int32_t* counts, const int32_t* offsets,
+                       const void* W13, const void* W2, void* h, void* y_sorted, void* ws,
+                       cudaStream_t st) {
   using namespace gg;
   if (!get_encoder()) return MOE_E_CUDA;
   if (set_smem_attr() != MOE_OK) return MOE_E_CUDA;
@@ -540,10 +695,18 @@ int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
   const uint64_t rows_h = uint64_t(R) + (c.has_shared ? c.T : 0);
 
   CUtensorMap mA1, mA1s, mA1h, mA1sh, mB1, mA2, mA2h, mB2;
-  const void* a1s = c.has_shared ? x : x_sorted;
-  const uint64_t a1s_rows = c.has_shared ? uint64_t(c.T) : uint64_t(R);
-  if (!make_map(&mA1, x_sorted, uint64_t(R), c.d, BM)) return MOE_E_CUDA;
-  if (!make_map(&mA1h, x_sorted, uint64_t(R), c.d, BM / 2)) return MOE_E_CUDA;
+  // the shared expert's rows (or, with no shared expert, any valid map: unused)
+  const bool a1s_x = c.has_shared || x_sorted == nullptr;
+  const void* a1s = a1s_x ? x : x_sorted;
+  const uint64_t a1s_rows = a1s_x ? uint64_t(c.T) : uint64_t(R);
+  if (gather_order) {
+    // routed rows gathered from the token rows: a map whose box is one row high
+    if (!make_map(&mA1, x, uint64_t(c.T), c.d, 1)) return MOE_E_CUDA;
+    mA1h = mA1;
+  } else {
+    if (!make_map(&mA1, x_sorted, uint64_t(R), c.d, BM)) return MOE_E_CUDA;
+    if (!make_map(&mA1h, x_sorted, uint64_t(R), c.d, BM / 2)) return MOE_E_CUDA;
+  }
   if (!make_map(&mA1s, a1s, a1s_rows, c.d, BM)) return MOE_E_CUDA;
   if (!make_map(&mA1sh, a1s, a1s_rows, c.d, BM / 2)) return MOE_E_CUDA;
   if (!make_map(&mB1, W13, uint64_t(n_exp) * 2 * c.f, c.d, BN)) return MOE_E_CUDA;
@@ -572,11 +735,14 @@ int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
   p1.out = static_cast<__nv_bfloat16*>(h);
   p1.ld_out = c.f;
   p1.status = ws_ptr<int>(ws, L.status);
+  p1.gather_order = gather_order;
+  p1.gather_k = c.k;
   const long long t1 = mt_ub * ((p1.N + BN - 1) / BN);
   const int grid1 = int(t1 < sms ? t1 : sms);
   grouped_gemm_kernel<<<grid1, THREADS, DYN_SMEM, st>>>(mA1, mA1s, mA1h, mA1sh, mB1, p1);
 
   GroupedParams p2 = p1;
+  p2.gather_order = nullptr;
   p2.K = c.f;
   p2.N = c.d;
   p2.mode = kEpiBf16;
@@ -588,6 +754,170 @@ int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
   grouped_gemm_kernel<<<grid2, THREADS, DYN_SMEM, st>>>(mA2, mA2, mA2h, mA2h, mB2, p2);
   note_launches(2);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_E_CUDA;
+}
+
+}  // namespace moe
+
+namespace moe {
+
+// Rows of the transposed-operand buffers of the weight gradients: an upper
+// bound on the padded reduction length, sum over segments of roundup(kept, 64).
+size_t backward_kpad_bound(const moe_cfg& c) {
+  const size_t R = c.capacity ? size_t(c.E) * c.capacity : size_t(c.T) * c.k;
+  const size_t ub = R + size_t(c.E) * 64 + (c.has_shared ? ((size_t(c.T) + 63) & ~size_t(63)) : 0);
+  return (ub + 63) & ~size_t(63);
+}
+
+// Backward workspace: g1 and dg1 [R + T, 2f] bf16, the padded segment offsets,
+// and one region reused for the transposed operands of both weight gradients.
+BwdLayout backward_layout(const moe_cfg& c) {
+  BwdLayout L;
+  const size_t rows = (c.capacity ? size_t(c.E) * c.capacity : size_t(c.T) * c.k) +
+                      (c.has_shared ? size_t(c.T) : 0);
+  const size_t kub = backward_kpad_bound(c);
+  size_t off = 0;
+  L.g1 = off;   off += align256(rows * 2 * c.f * 2);
+  L.dg1 = off;  off += align256(rows * 2 * c.f * 2);
+  L.kpad = off; off += align256(size_t(c.E + 2) * 4);
+  L.tr = off;
+  const size_t w2 = size_t(c.d + c.f), w13 = size_t(2 * c.f + c.d);
+  off += align256((w2 > w13 ? w2 : w13) * kub * 2);
+  L.total = off;
+  L.kub = kub;
+  return L;
+}
+
+int launch_grouped_ffn_backward(const moe_cfg& c, const void* x_sorted, const void* x,
+                                const int32_t* counts, const int32_t* offsets, const void* W13,
+                                const void* W13t, const void* W2t, const void* h,
+                                const void* d_o, void* dx_sorted, void* dW13, void* dW2,
+                                void* bws, void* ws, cudaStream_t st) {
+  using namespace gg;
+  if (!get_encoder()) return MOE_E_CUDA;
+  if (set_smem_attr() != MOE_OK) return MOE_E_CUDA;
+  const WsLayout L = ws_layout(c);
+  const BwdLayout B = backward_layout(c);
+  const int R = c.capacity ? c.E * c.capacity : c.T * c.k;
+  const int n_exp = c.E + c.has_shared;
+  const uint64_t rows_h = uint64_t(R) + (c.has_shared ? c.T : 0);
+  char* bw = static_cast<char*>(bws);
+  __nv_bfloat16* g1 = reinterpret_cast<__nv_bfloat16*>(bw + B.g1);
+  __nv_bfloat16* dg1 = reinterpret_cast<__nv_bfloat16*>(bw + B.dg1);
+  int32_t* kpad = reinterpret_cast<int32_t*>(bw + B.kpad);
+  __nv_bfloat16* trA = reinterpret_cast<__nv_bfloat16*>(bw + B.tr);
+  const size_t kub = B.kub;
+
+  GroupedParams base{};
+  base.counts = counts;
+  base.offsets = offsets;
+  base.E = c.E;
+  base.capacity = c.capacity;
+  base.has_shared = c.has_shared;
+  base.T = c.T;
+  base.R = R;
+  base.k_passes = 1;
+  base.status = ws_ptr<int>(ws, L.status);
+
+  // 1. g1 = x W13^T (recomputed; routed rows from x_sorted, shared rows from x)
+  {
+    CUtensorMap mA, mAh, mAs, mAsh, mB;
+    const bool sx = c.has_shared;
+    if (!make_map(&mA, x_sorted, uint64_t(R), c.d, BM)) return MOE_E_CUDA;
+    if (!make_map(&mAh, x_sorted, uint64_t(R), c.d, BM / 2)) return MOE_E_CUDA;
+    if (!make_map(&mAs, sx ? x : x_sorted, sx ? uint64_t(c.T) : uint64_t(R), c.d, BM))
+      return MOE_E_CUDA;
+    if (!make_map(&mAsh, sx ? x : x_sorted, sx ? uint64_t(c.T) : uint64_t(R), c.d, BM / 2))
+      return MOE_E_CUDA;
+    if (!make_map(&mB, W13, uint64_t(n_exp) * 2 * c.f, c.d, BN)) return MOE_E_CUDA;
+    GroupedParams p = base;
+    p.K = c.d;
+    p.N = 2 * c.f;
+    p.mode = kEpiBf16;
+    p.shared_a_separate = 1;
+    p.out = g1;
+    p.ld_out = 2 * c.f;
+    MOE_TRY_INTERNAL(launch_gg(rows_h, n_exp, mA, mAs, mAh, mAsh, mB, p, st));
+  }
+  // 2. dh = d_o W2 (B = W2^T per expert, N = f, K = d); the epilogue applies the
+  //    SwiGLU derivative with g1 and writes dg1 (packed like W13)
+  {
+    CUtensorMap mA, mAh, mB;
+    if (!make_map(&mA, d_o, rows_h, c.d, BM)) return MOE_E_CUDA;
+    if (!make_map(&mAh, d_o, rows_h, c.d, BM / 2)) return MOE_E_CUDA;
+    if (!make_map(&mB, W2t, uint64_t(n_exp) * c.f, c.d, BN)) return MOE_E_CUDA;
+    GroupedParams p = base;
+    p.K = c.d;
+    p.N = c.f;
+    p.mode = kEpiSwigluBwd;
+    p.shared_a_separate = 0;
+    p.aux = g1;
+    p.ld_aux = 2 * c.f;
+    p.out = dg1;
+    p.ld_out = 2 * c.f;
+    MOE_TRY_INTERNAL(launch_gg(rows_h, n_exp, mA, mA, mAh, mAh, mB, p, st));
+  }
+  // 3. dx_sorted = dg1 W13 (B = W13^T per expert, N = d, K = 2f)
+  {
+    CUtensorMap mA, mAh, mB;
+    if (!make_map(&mA, dg1, rows_h, 2 * c.f, BM)) return MOE_E_CUDA;
+    if (!make_map(&mAh, dg1, rows_h, 2 * c.f, BM / 2)) return MOE_E_CUDA;
+    if (!make_map(&mB, W13t, uint64_t(n_exp) * c.d, 2 * c.f, BN)) return MOE_E_CUDA;
+    GroupedParams p = base;
+    p.K = 2 * c.f;
+    p.N = c.d;
+    p.mode = kEpiBf16;
+    p.shared_a_separate = 0;
+    p.out = static_cast<__nv_bfloat16*>(dx_sorted);
+    p.ld_out = c.d;
+    MOE_TRY_INTERNAL(launch_gg(rows_h, n_exp, mA, mA, mAh, mAh, mB, p, st));
+  }
+  // 4. weight gradients, each over its expert's rows
+  MOE_TRY_INTERNAL(launch_kpad_offsets(c, counts, kpad, st));
+  const __nv_bfloat16* hb = static_cast<const __nv_bfloat16*>(h);
+  const __nv_bfloat16* dob = static_cast<const __nv_bfloat16*>(d_o);
+  __nv_bfloat16* trB = trA + size_t(c.d) * kub;  // after d_o^T [d, kub]
+  MOE_TRY_INTERNAL(launch_transpose_segments(c, d_o, dob + size_t(R) * c.d, c.d, offsets, counts,
+                                             kpad, trA, kub, st));
+  MOE_TRY_INTERNAL(launch_transpose_segments(c, h, hb + size_t(R) * c.f, c.f, offsets, counts,
+                                             kpad, trB, kub, st));
+  {
+    // dW2[g] = d_o^T h: [d, f] per segment
+    CUtensorMap mA, mAh, mB;
+    if (!make_map(&mA, trA, uint64_t(c.d), kub, BM)) return MOE_E_CUDA;
+    if (!make_map(&mAh, trA, uint64_t(c.d), kub, BM / 2)) return MOE_E_CUDA;
+    if (!make_map(&mB, trB, uint64_t(c.f), kub, BN)) return MOE_E_CUDA;
+    GroupedParams p = base;
+    p.K = BK;
+    p.N = c.f;
+    p.mode = kEpiBf16;
+    p.kpad_off = kpad;
+    p.m_out = c.d;
+    p.out = static_cast<__nv_bfloat16*>(dW2);
+    p.ld_out = c.f;
+    MOE_TRY_INTERNAL(launch_gg(int64_t(n_exp) * c.d, n_exp, mA, mA, mAh, mAh, mB, p, st));
+  }
+  __nv_bfloat16* trC = trA + size_t(2 * c.f) * kub;  // after dg1^T [2f, kub]
+  MOE_TRY_INTERNAL(launch_transpose_segments(c, dg1, dg1 + size_t(R) * 2 * c.f, 2 * c.f, offsets,
+                                             counts, kpad, trA, kub, st));
+  MOE_TRY_INTERNAL(launch_transpose_segments(c, x_sorted, c.has_shared ? x : x_sorted, c.d,
+                                             offsets, counts, kpad, trC, kub, st));
+  {
+    // dW13[g] = dg1^T x: [2f, d] per segment (rows packed like W13)
+    CUtensorMap mA, mAh, mB;
+    if (!make_map(&mA, trA, uint64_t(2 * c.f), kub, BM)) return MOE_E_CUDA;
+    if (!make_map(&mAh, trA, uint64_t(2 * c.f), kub, BM / 2)) return MOE_E_CUDA;
+    if (!make_map(&mB, trC, uint64_t(c.d), kub, BN)) return MOE_E_CUDA;
+    GroupedParams p = base;
+    p.K = BK;
+    p.N = c.d;
+    p.mode = kEpiBf16;
+    p.kpad_off = kpad;
+    p.m_out = 2 * c.f;
+    p.out = static_cast<__nv_bfloat16*>(dW13);
+    p.ld_out = c.d;
+    MOE_TRY_INTERNAL(launch_gg(int64_t(n_exp) * 2 * c.f, n_exp, mA, mA, mAh, mAh, mB, p, st));
+  }
+  return MOE_OK;
 }
 
 }  // namespace moe

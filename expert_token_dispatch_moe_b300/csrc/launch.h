@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include "../../include/moe.h"
+#include "common.cuh"
 
 namespace moe {
 
@@ -30,8 +31,9 @@ int launch_ep_layout(const moe_cfg& c, const int32_t* idx, const int32_t* offset
                      int32_t* send_idx, const void* x, void* send_buf, void* ws, cudaStream_t st);
 int launch_pack_w13(const moe_cfg& c, const void* W1, const void* W3, void* W13, cudaStream_t st);
 int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
-                       const int32_t* counts, const int32_t* offsets, const void* W13,
-                       const void* W2, void* h, void* y_sorted, void* ws, cudaStream_t st);
+                       const int32_t* gather_order, const int32_t* counts, const int32_t* offsets,
+                       const void* W13, const void* W2, void* h, void* y_sorted, void* ws,
+                       cudaStream_t st);
 int launch_combine(const moe_cfg& c, const void* y_sorted, const int32_t* inv, const float* gate,
                    void* y, cudaStream_t st);
 
@@ -49,6 +51,25 @@ int launch_fp8_pack(const moe_cfg& c, const void* x, const int32_t* send_idx, vo
                     float* send_scale, void* ws, cudaStream_t st);
 int launch_fp8_recv(const moe_cfg& c, const void* send_fp8, const float* send_scale,
                     const int32_t* send_idx, const int32_t* inv, void* x_sorted, cudaStream_t st);
+
+// Backward of the layer (routing held fixed).
+size_t backward_kpad_bound(const moe_cfg& c);
+BwdLayout backward_layout(const moe_cfg& c);
+int launch_combine_backward(const moe_cfg& c, const void* dy, const void* y_sorted,
+                            const int32_t* inv, const float* gate, void* d_o, float* dgate,
+                            cudaStream_t st);
+int launch_pack_backward(const moe_cfg& c, const void* W13, const void* W2, void* W13t, void* W2t,
+                         cudaStream_t st);
+int launch_kpad_offsets(const moe_cfg& c, const int32_t* counts, int32_t* kpad_off,
+                        cudaStream_t st);
+int launch_transpose_segments(const moe_cfg& c, const void* src, const void* src_shared, int C,
+                              const int32_t* offsets, const int32_t* counts,
+                              const int32_t* kpad_off, void* dst, size_t ld_dst, cudaStream_t st);
+int launch_grouped_ffn_backward(const moe_cfg& c, const void* x_sorted, const void* x,
+                                const int32_t* counts, const int32_t* offsets, const void* W13,
+                                const void* W13t, const void* W2t, const void* h,
+                                const void* d_o, void* dx_sorted, void* dW13, void* dW2,
+                                void* bws, void* ws, cudaStream_t st);
 
 // Row move shared by the permute and the send-buffer fill: for each token t
 // and slot j, copy x[t] to dst[rows[t*k + j]] when that row is >= 0.

@@ -172,7 +172,9 @@ MOE_API int moe_permute(const moe_cfg* c, const moe_bf16* x, const int32_t* topk
                         moe_bf16* x_sorted, void* ws, size_t ws_bytes, void* stream) {
   reset_launches();
   MOE_TRY(moe_validate_cfg(c));
-  MOE_TRY(check_ptrs({x, topk_idx, counts, offsets, order, inv, x_sorted}));
+  MOE_TRY(check_ptrs({topk_idx, counts, offsets, order, inv}));
+  MOE_TRY(check_opt({x, x_sorted}));
+  if ((x == nullptr) != (x_sorted == nullptr)) return MOE_E_NULL;
   MOE_TRY(check_ws(c, ws, ws_bytes));
   MOE_TRY(device_ok());
   return launch_permute(*c, x, topk_idx, counts, offsets, order, inv, x_sorted, ws,
@@ -247,7 +249,22 @@ MOE_API int moe_grouped_ffn(const moe_cfg* c, const moe_bf16* x_sorted, const mo
   else MOE_TRY(check_opt({x}));
   MOE_TRY(check_ws(c, ws, ws_bytes));
   MOE_TRY(device_ok());
-  return launch_grouped_ffn(*c, x_sorted, x, counts, offsets, W13, W2, h, y_sorted, ws,
+  return launch_grouped_ffn(*c, x_sorted, x, nullptr, counts, offsets, W13, W2, h, y_sorted, ws,
+                            static_cast<cudaStream_t>(stream));
+}
+
+MOE_API int moe_grouped_ffn_gather(const moe_cfg* c, const moe_bf16* x, const int32_t* order,
+                                   const int32_t* counts, const int32_t* offsets,
+                                   const moe_bf16* W13, const moe_bf16* W2, moe_bf16* h,
+                                   moe_bf16* y_sorted, void* ws, size_t ws_bytes, void* stream) {
+  reset_launches();
+  MOE_TRY(moe_validate_cfg(c));
+  if (c->f < 128 || c->f % 128) return MOE_E_SHAPE;
+  if (c->E + c->has_shared > 1025) return MOE_E_SHAPE;
+  MOE_TRY(check_ptrs({x, order, counts, offsets, W13, W2, h, y_sorted}));
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  MOE_TRY(device_ok());
+  return launch_grouped_ffn(*c, nullptr, x, order, counts, offsets, W13, W2, h, y_sorted, ws,
                             static_cast<cudaStream_t>(stream));
 }
 
@@ -294,6 +311,65 @@ MOE_API int moe_eplb_dispatch(const moe_cfg* c, const int32_t* topk_idx, const i
   MOE_TRY(device_ok());
   return launch_eplb_dispatch(*c, topk_idx, inv, offsets, counts, copies, copy_offset, copy_rank,
                               dest_rank, count_mat, static_cast<cudaStream_t>(stream));
+}
+
+MOE_API int moe_pack_backward(const moe_cfg* c, const moe_bf16* W13, const moe_bf16* W2,
+                              moe_bf16* W13t, moe_bf16* W2t, void* stream) {
+  reset_launches();
+  MOE_TRY(moe_validate_cfg(c));
+  if (c->f < 128 || c->f % 128) return MOE_E_SHAPE;
+  MOE_TRY(check_ptrs({W13, W2, W13t, W2t}));
+  MOE_TRY(device_ok());
+  return launch_pack_backward(*c, W13, W2, W13t, W2t, static_cast<cudaStream_t>(stream));
+}
+
+MOE_API int moe_combine_backward(const moe_cfg* c, const moe_bf16* dy, const moe_bf16* y_sorted,
+                                 const int32_t* inv, const float* topk_gate, moe_bf16* d_o,
+                                 float* dgate, void* stream) {
+  reset_launches();
+  MOE_TRY(moe_validate_cfg(c));
+  MOE_TRY(check_ptrs({dy, y_sorted, inv, topk_gate, d_o, dgate}));
+  MOE_TRY(device_ok());
+  return launch_combine_backward(*c, dy, y_sorted, inv, topk_gate, d_o, dgate,
+                                 static_cast<cudaStream_t>(stream));
+}
+
+MOE_API size_t moe_backward_workspace_bytes(const moe_cfg* c) {
+  if (moe_validate_cfg(c) != MOE_OK || c->f < 128 || c->f % 128) return 0;
+  return backward_layout(*c).total;
+}
+
+MOE_API int moe_grouped_ffn_backward(const moe_cfg* c, const moe_bf16* x_sorted, const moe_bf16* x,
+                                     const int32_t* counts, const int32_t* offsets,
+                                     const moe_bf16* W13, const moe_bf16* W13t,
+                                     const moe_bf16* W2t, const moe_bf16* h,
+                                     const moe_bf16* d_o, moe_bf16* dx_sorted, moe_bf16* dW13,
+                                     moe_bf16* dW2, void* bws, size_t bws_bytes, void* ws,
+                                     size_t ws_bytes, void* stream) {
+  reset_launches();
+  MOE_TRY(moe_validate_cfg(c));
+  if (c->f < 128 || c->f % 128) return MOE_E_SHAPE;
+  if (c->E + c->has_shared > 1025) return MOE_E_SHAPE;
+  MOE_TRY(check_ptrs({x_sorted, counts, offsets, W13, W13t, W2t, h, d_o, dx_sorted, dW13, dW2}));
+  if (c->has_shared) MOE_TRY(check_ptrs({x}));
+  else MOE_TRY(check_opt({x}));
+  if (!bws) return MOE_E_WORKSPACE;
+  if (!aligned16(bws)) return MOE_E_ALIGN;
+  if (bws_bytes < backward_layout(*c).total) return MOE_E_WORKSPACE;
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  MOE_TRY(device_ok());
+  return launch_grouped_ffn_backward(*c, x_sorted, x, counts, offsets, W13, W13t, W2t, h, d_o,
+                                     dx_sorted, dW13, dW2, bws, ws,
+                                     static_cast<cudaStream_t>(stream));
+}
+
+MOE_API int moe_permute_backward(const moe_cfg* c, const moe_bf16* dx_sorted, const int32_t* inv,
+                                 moe_bf16* dx, void* stream) {
+  reset_launches();
+  MOE_TRY(moe_validate_cfg(c));
+  MOE_TRY(check_ptrs({dx_sorted, inv, dx}));
+  MOE_TRY(device_ok());
+  return launch_combine(*c, dx_sorted, inv, nullptr, dx, static_cast<cudaStream_t>(stream));
 }
 
 MOE_API int moe_get_device_status(void* ws, void* stream) {

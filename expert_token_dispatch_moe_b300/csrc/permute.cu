@@ -225,8 +225,8 @@ __global__ void __launch_bounds__(256) row_scatter_kernel(const uint4* __restric
   }
 }
 
-// Capacity mode: zero the padding rows of the grouped buffer and set their
-// order entry to -1.  Row r belongs to expert e = r / cap and is padding when
+// Capacity mode: set the order entry of the grouped buffer's padding rows to
+// -1 and zero the rows (when the buffer is given).  Row r belongs to expert e = r / cap and is padding when
 // r - e*cap >= min(counts[e], cap).  One warp per row, grid-stride.
 __global__ void __launch_bounds__(256) perm_pad_kernel(const int32_t* __restrict__ counts,
                                                        int capacity, int R, int vec_per_row,
@@ -238,6 +238,7 @@ __global__ void __launch_bounds__(256) perm_pad_kernel(const int32_t* __restrict
     const int e = r / capacity;
     if (r - e * capacity < min(__ldg(counts + e), capacity)) continue;
     if (lane == 0) order[r] = -1;
+    if (x_sorted == nullptr) continue;
     uint4* row = x_sorted + size_t(r) * vec_per_row;
     for (int v = lane; v < vec_per_row; v += 32) row[v] = make_uint4(0, 0, 0, 0);
   }
@@ -384,6 +385,7 @@ int launch_permute(const moe_cfg& c, const void* x, const int32_t* idx, int32_t*
     note_launches(1);
   }
   if (cudaGetLastError() != cudaSuccess) return MOE_E_CUDA;
+  if (x_sorted == nullptr) return MOE_OK;  // indices only: the rows are gathered later
   return launch_row_scatter(x, c.T, c.d, c.k, inv, x_sorted, st);
 }
 

@@ -14,9 +14,11 @@ from __future__ import annotations
 
 import torch
 
-from . import (MoeCfg, moe_combine, moe_ep_layout, moe_grouped_ffn, moe_grouped_rows,
-               moe_last_launch_count, moe_pack_router, moe_pack_w13, moe_permute, moe_route,
-               moe_router_logits, moe_workspace_bytes, moe_workspace_init)
+from . import (MoeCfg, moe_backward_workspace_bytes, moe_combine, moe_combine_backward,
+               moe_ep_layout, moe_grouped_ffn, moe_grouped_ffn_backward, moe_grouped_ffn_gather,
+               moe_grouped_rows, moe_last_launch_count, moe_pack_backward, moe_pack_router,
+               moe_pack_w13, moe_permute, moe_permute_backward, moe_route, moe_router_logits,
+               moe_workspace_bytes, moe_workspace_init)
 
 # Routers with at least this many experts run on the tensor cores (three-term
 # bf16 split of the fp32 weights); smaller ones are bandwidth-bound SIMT dot
@@ -26,7 +28,9 @@ TC_ROUTER_MIN_E = 17
 
 class MoELayer:
     def __init__(self, cfg, W1, W3, W2, W_r=None, logit_bias=None, selection_bias=None,
-                 device=None, with_send_buf=True, tc_router=None):
+                 device=None, with_send_buf=True, tc_router=None, gather=False):
+        """gather=True: the permute computes indices only and GEMM 1 gathers its
+        rows from x (moe_grouped_ffn_gather); x_sorted is not written."""
         self.cfg = cfg if isinstance(cfg, MoeCfg) else MoeCfg.from_layer(cfg)
         c = self.cfg
         dev = torch.device(device or "cuda")
@@ -67,7 +71,10 @@ class MoELayer:
         self.y = torch.empty(c.T, c.d, dtype=bf16, device=dev)
         self.ws = torch.zeros(moe_workspace_bytes(c), dtype=torch.uint8, device=dev)
         moe_workspace_init(c, self.ws)
+        self.gather = gather
         self.launches_per_forward = None
+        self.launches_per_backward = None
+        self.W13t = None        # backward buffers, allocated on the first backward
 
     def forward(self, x, scores=None):
         """Run the layer on device tokens x (bf16 [T, d]); returns self.y.
@@ -83,15 +90,23 @@ class MoELayer:
             scores = self.scores
         moe_route(c, scores, self.selection_bias, self.topk_idx, self.topk_gate)
         n += moe_last_launch_count()
-        moe_permute(c, x, self.topk_idx, self.counts, self.offsets, self.order, self.inv,
-                    self.x_sorted, self.ws)
+        if self.gather:
+            moe_permute(c, None, self.topk_idx, self.counts, self.offsets, self.order, self.inv,
+                        None, self.ws)
+        else:
+            moe_permute(c, x, self.topk_idx, self.counts, self.offsets, self.order, self.inv,
+                        self.x_sorted, self.ws)
         n += moe_last_launch_count()
         moe_ep_layout(c, self.topk_idx, self.offsets, self.inv, self.count_mat, self.send_off,
                       self.recv_off, self.send_idx, x if self.send_buf is not None else None,
                       self.send_buf, self.ws)
         n += moe_last_launch_count()
-        moe_grouped_ffn(c, self.x_sorted, x if c.has_shared else None, self.counts, self.offsets,
-                        self.W13, self.W2, self.h, self.y_sorted, self.ws)
+        if self.gather:
+            moe_grouped_ffn_gather(c, x, self.order, self.counts, self.offsets, self.W13, self.W2,
+                                   self.h, self.y_sorted, self.ws)
+        else:
+            moe_grouped_ffn(c, self.x_sorted, x if c.has_shared else None, self.counts,
+                            self.offsets, self.W13, self.W2, self.h, self.y_sorted, self.ws)
         n += moe_last_launch_count()
         moe_combine(c, self.y_sorted, self.inv, self.topk_gate, self.y)
         n += moe_last_launch_count()
@@ -99,6 +114,47 @@ class MoELayer:
         return self.y
 
     __call__ = forward
+
+    def _backward_buffers(self):
+        c, dev, bf16 = self.cfg, self.device, torch.bfloat16
+        n_exp = c.E + c.has_shared
+        rows = moe_grouped_rows(c)
+        self.W13t = torch.empty(n_exp, c.d, 2 * c.f, dtype=bf16, device=dev)
+        self.W2t = torch.empty(n_exp, c.f, c.d, dtype=bf16, device=dev)
+        moe_pack_backward(c, self.W13, self.W2, self.W13t, self.W2t)
+        self.d_o = torch.empty(rows, c.d, dtype=bf16, device=dev)
+        self.dx_sorted = torch.empty(rows, c.d, dtype=bf16, device=dev)
+        self.dW13 = torch.empty(n_exp, 2 * c.f, c.d, dtype=bf16, device=dev)
+        self.dW2 = torch.empty(n_exp, c.d, c.f, dtype=bf16, device=dev)
+        self.dgate = torch.empty(c.T, c.k, dtype=torch.float32, device=dev)
+        self.dx = torch.empty(c.T, c.d, dtype=bf16, device=dev)
+        self.bws = torch.empty(moe_backward_workspace_bytes(c), dtype=torch.uint8, device=dev)
+
+    def backward(self, x, dy):
+        """Gradients of the last forward (rows path) for output gradient dy
+        (bf16 [T, d]), routing held fixed: returns self.dx and leaves self.dW13
+        (packed like W13), self.dW2 and self.dgate."""
+        if self.gather:
+            raise RuntimeError("backward needs the forward's x_sorted (gather=False)")
+        c = self.cfg
+        if self.W13t is None:
+            self._backward_buffers()
+        moe_combine_backward(c, dy, self.y_sorted, self.inv, self.topk_gate, self.d_o, self.dgate)
+        n = moe_last_launch_count()
+        moe_grouped_ffn_backward(c, self.x_sorted, x if c.has_shared else None, self.counts,
+                                 self.offsets, self.W13, self.W13t, self.W2t, self.h, self.d_o,
+                                 self.dx_sorted, self.dW13, self.dW2, self.bws, self.ws)
+        n += moe_last_launch_count()
+        moe_permute_backward(c, self.dx_sorted, self.inv, self.dx)
+        n += moe_last_launch_count()
+        self.launches_per_backward = n
+        return self.dx
+
+    def unpacked_dW13(self):
+        """(dW1, dW3) [E + has_shared, f, d] from the packed dW13."""
+        n, f2, d = self.dW13.shape
+        blk = self.dW13.view(n, f2 // 256, 2, 128, d)
+        return blk[:, :, 0].reshape(n, f2 // 2, d), blk[:, :, 1].reshape(n, f2 // 2, d)
 
     def forward_host(self, x_host, y_host, x_dev=None):
         """End-to-end call with host buffers: copies pinned host x to the

@@ -144,7 +144,9 @@ int moe_route(const moe_cfg* cfg, const float* scores, const float* bias,
  *             exclusive prefix sum of counts, offsets[E] = A; capacity: e*cap)
  *   order     int32 [R] out: row -> assignment a (-1 for a padding row)
  *   inv       int32 [A] out: assignment -> row (-1 when dropped)
- *   x_sorted  bf16 [R, d] out: x_sorted[inv[a]] = x[a / k]; padding rows zero
+ *   x_sorted  bf16 [R, d] out: x_sorted[inv[a]] = x[a / k]; padding rows zero.
+ *             x and x_sorted may both be NULL: the indices are computed and no
+ *             row moves (for moe_grouped_ffn_gather, which reads rows from x).
  *   ws        workspace; keeps the per-(source rank, expert) histogram that
  *             moe_ep_layout reads
  * Capacity: expert e keeps its first `capacity` assignments in increasing a. */
@@ -258,6 +260,20 @@ int moe_grouped_ffn(const moe_cfg* cfg, const moe_bf16* x_sorted, const moe_bf16
                     const moe_bf16* W13, const moe_bf16* W2, moe_bf16* h,
                     moe_bf16* y_sorted, void* ws, size_t ws_bytes, void* stream);
 
+/* moe_grouped_ffn with the permute's row move fused into GEMM 1's operand
+ * loads ("Token permutation and grouped GEMMs": production kernels fuse the
+ * permutation into the grouped GEMM's loads, saving a full read and write of
+ * the (T*k, d) tensor).  Row r of expert e's segment is gathered from token
+ * order[r] / k of x by four-row tensor-memory-access copies; no x_sorted
+ * buffer is read.
+ *   x       bf16 [T, d] (also the shared expert's rows)
+ *   order   int32 [R] from moe_permute (row -> assignment)
+ *   other arguments and outputs as for moe_grouped_ffn. */
+int moe_grouped_ffn_gather(const moe_cfg* cfg, const moe_bf16* x, const int32_t* order,
+                           const int32_t* counts, const int32_t* offsets, const moe_bf16* W13,
+                           const moe_bf16* W2, moe_bf16* h, moe_bf16* y_sorted, void* ws,
+                           size_t ws_bytes, void* stream);
+
 /* Step 7, unpermute and weight ("Expert parallelism", step 7: undo the sort
  * and scatter-add each row into its token with its gate).  Computed as a
  * per-token gather in slot order j = 0..k-1 with fp32 accumulation (the same
@@ -268,6 +284,67 @@ int moe_grouped_ffn(const moe_cfg* cfg, const moe_bf16* x_sorted, const moe_bf16
  *   y        bf16 [T, d] out */
 int moe_combine(const moe_cfg* cfg, const moe_bf16* y_sorted, const int32_t* inv,
                 const float* topk_gate, moe_bf16* y, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Backward of the layer with the routing held fixed ("Expert parallelism":
+ * the dispatch and combine run twice more in the backward pass).  Order:
+ *   moe_combine_backward -> moe_grouped_ffn_backward -> moe_permute_backward.
+ * Gradients are bf16 with fp32 accumulation.  The gradient with respect to
+ * the router scores (through the gates) is left to the caller: dgate is
+ * returned.
+ * ------------------------------------------------------------------------ */
+
+/* One-time transposed copies of the expert weights for the backward:
+ *   W13  bf16 [E + has_shared, 2f, d] (moe_pack_w13) -> W13t [E + has_shared, d, 2f]
+ *   W2   bf16 [E + has_shared, d, f]                 -> W2t  [E + has_shared, f, d] */
+int moe_pack_backward(const moe_cfg* cfg, const moe_bf16* W13, const moe_bf16* W2,
+                      moe_bf16* W13t, moe_bf16* W2t, void* stream);
+
+/* Step 7 backward: the combine's gradient is a dispatch of dy.
+ *   dy        bf16 [T, d]: gradient of the layer output
+ *   y_sorted  bf16 [R + has_shared*T, d]: the forward's expert outputs
+ *   inv, topk_gate: the forward's (moe_permute, moe_route)
+ *   d_o       bf16 [R + has_shared*T, d] out: kept row of assignment a =
+ *             topk_gate[a] * dy[a / k]; shared row R + t = dy[t]; padding rows
+ *             are not written
+ *   dgate     fp32 [T, k] out: <dy[t], y_sorted[inv[a]]> (fp32 accumulation),
+ *             0 for dropped assignments */
+int moe_combine_backward(const moe_cfg* cfg, const moe_bf16* dy, const moe_bf16* y_sorted,
+                         const int32_t* inv, const float* topk_gate, moe_bf16* d_o,
+                         float* dgate, void* stream);
+
+/* Bytes of the backward workspace of moe_grouped_ffn_backward (0 on an
+ * invalid configuration).  Host only. */
+size_t moe_backward_workspace_bytes(const moe_cfg* cfg);
+
+/* Step 5 backward, on the tensor cores:
+ *   g1 = x W13^T (recomputed into the backward workspace),
+ *   dg1 = SwiGLU'(g1) applied to d_o W2 (fused into that product's epilogue;
+ *         du = dh v s (1 + u (1 - s)), dv = dh u s, s = sigmoid(u)),
+ *   dx_sorted = dg1 W13,
+ *   dW2[e] = d_o^T h and dW13[e] = dg1^T x over expert e's kept rows (the
+ *   operands transposed into the workspace, each expert's rows starting on a
+ *   64-column boundary, zero-padded).
+ *   x_sorted, x, counts, offsets, W13 as for moe_grouped_ffn; W13t, W2t from
+ *   moe_pack_backward; h the forward's [R + has_shared*T, f]; d_o from
+ *   moe_combine_backward.
+ *   dx_sorted bf16 [R + has_shared*T, d] out (kept and shared rows)
+ *   dW13      bf16 [E + has_shared, 2f, d] out, rows packed like W13
+ *   dW2       bf16 [E + has_shared, d, f] out (zero for an expert with no rows)
+ *   bws       backward workspace of moe_backward_workspace_bytes(cfg) bytes
+ *   ws        the layer workspace (status word). */
+int moe_grouped_ffn_backward(const moe_cfg* cfg, const moe_bf16* x_sorted, const moe_bf16* x,
+                             const int32_t* counts, const int32_t* offsets,
+                             const moe_bf16* W13, const moe_bf16* W13t, const moe_bf16* W2t,
+                             const moe_bf16* h, const moe_bf16* d_o, moe_bf16* dx_sorted,
+                             moe_bf16* dW13, moe_bf16* dW2, void* bws, size_t bws_bytes,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/* Step 2 backward: the permute's gradient is a combine with unit gates,
+ *   dx[t] = sum over kept j of dx_sorted[inv[t*k+j]] (+ dx_sorted[R + t] with a
+ *   shared expert), fp32 accumulation in slot order, rounded to bf16. */
+int moe_permute_backward(const moe_cfg* cfg, const moe_bf16* dx_sorted, const int32_t* inv,
+                         moe_bf16* dx, void* stream);
 
 /* Load balancing, step 1: the auxiliary-loss-free bias update ("05 - Expert
  * Parallelism (MoE)", "Load balancing" (b)).  After a step, with the tokens
