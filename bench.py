@@ -144,7 +144,8 @@ def _algorithmic(cfg, counts_np, gather=False):
 
 def _time_extras(m, layer, c, cfg, x, st, flush, counts, pk, reps):
     """Calls outside the layer step, timed alone with CUDA events (L2 flushed
-    before each): the FP8 dispatch pair and the load-balancing kernels."""
+    before each): the layer's backward, the FP8 dispatch pair and the
+    load-balancing kernels."""
     dev = x.device
 
     def timed(fn):
@@ -160,7 +161,60 @@ def _time_extras(m, layer, c, cfg, x, st, flush, counts, pk, reps):
         return float(np.mean([a.elapsed_time(b) for a, b in out[1:]]))
 
     A, d = cfg.A, cfg.d
+    out = {}
+    # backward of the layer (routing fixed), on the forward's buffers
+    if not layer.gather:
+        out.update(_time_backward(m, layer, c, cfg, x, st, flush, counts, pk, reps))
     send_fp8 = torch.empty(A, d, dtype=torch.uint8, device=dev)
+    return _time_fp8_and_balance(m, layer, c, cfg, x, st, flush, counts, pk, reps, timed, out,
+                                 send_fp8)
+
+
+def _time_backward(m, layer, c, cfg, x, st, flush, counts, pk, reps):
+    """The three backward calls after a fresh forward, timed per call."""
+    dev = x.device
+    A, d = cfg.A, cfg.d
+    out = {}
+    layer.forward(x)
+    gen = torch.Generator(device=dev).manual_seed(77)
+    dy = torch.randn(cfg.T, d, generator=gen, device=dev).to(torch.bfloat16)
+    layer.backward(x, dy)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    per = []
+    for _ in range(reps):
+        flush.zero_()
+        ev[0].record(st)
+        m.moe_combine_backward(c, dy, layer.y_sorted, layer.inv, layer.topk_gate, layer.d_o,
+                               layer.dgate)
+        ev[1].record(st)
+        m.moe_grouped_ffn_backward(c, layer.x_sorted, x if c.has_shared else None, layer.counts,
+                                   layer.offsets, layer.W13, layer.W13t, layer.W2t, layer.h,
+                                   layer.d_o, layer.dx_sorted, layer.dW13, layer.dW2, layer.bws,
+                                   layer.ws)
+        ev[2].record(st)
+        m.moe_permute_backward(c, layer.dx_sorted, layer.inv, layer.dx)
+        ev[3].record(st)
+        torch.cuda.synchronize(dev)
+        per.append([ev[i].elapsed_time(ev[i + 1]) for i in range(3)])
+    per = np.array(per).mean(axis=0)
+    kept = int(np.minimum(counts, cfg.capacity).sum()) if cfg.capacity else A
+    rows_ffn = kept + (cfg.T if cfg.has_shared else 0)
+    bw_flops = 12.0 * d * cfg.f * rows_ffn      # dh, dx (dgrad) + dW2, dW13 (wgrad)
+    tf = bw_flops / (per[1] * 1e-3) / 1e12
+    out["backward"] = {"ms": float(per.sum()), "combine_backward_ms": float(per[0]),
+                       "grouped_ffn_backward_ms": float(per[1]),
+                       "permute_backward_ms": float(per[2]),
+                       "ffn_backward_tflops": tf,
+                       "ffn_backward_frac_bf16_sustained": tf / (pk["bf16_tflops_sustained"]
+                                                                 or pk["bf16_tflops"]),
+                       "flops_counted": "12*d*f per kept row (the recomputed x*W13 is not credited)"}
+    return out
+
+
+def _time_fp8_and_balance(m, layer, c, cfg, x, st, flush, counts, pk, reps, timed, out,
+                          send_fp8):
+    dev = x.device
+    A, d = cfg.A, cfg.d
     send_scale = torch.empty(A, dtype=torch.float32, device=dev)
     ms_pack = timed(lambda: m.moe_ep_layout_fp8(c, layer.topk_idx, layer.offsets, layer.inv,
                                                 layer.count_mat, layer.send_off, layer.recv_off,
@@ -172,10 +226,10 @@ def _time_extras(m, layer, c, cfg, x, st, flush, counts, pk, reps):
     b_pack = cfg.T * d * 2 + A * d + 4 * A + 16 * A
     b_recv = A * d + 4 * A + 8 * A + kept * d * 2
     gbs = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
-    out = {"ep_layout_fp8": {"ms": ms_pack, "gbs": gbs(b_pack, ms_pack),
-                             "frac_hbm": gbs(b_pack, ms_pack) / pk["hbm_gbs"]},
-           "dispatch_recv_fp8": {"ms": ms_recv, "gbs": gbs(b_recv, ms_recv),
-                                 "frac_hbm": gbs(b_recv, ms_recv) / pk["hbm_gbs"]}}
+    out["ep_layout_fp8"] = {"ms": ms_pack, "gbs": gbs(b_pack, ms_pack),
+                            "frac_hbm": gbs(b_pack, ms_pack) / pk["hbm_gbs"]}
+    out["dispatch_recv_fp8"] = {"ms": ms_recv, "gbs": gbs(b_recv, ms_recv),
+                                "frac_hbm": gbs(b_recv, ms_recv) / pk["hbm_gbs"]}
     del send_fp8
     bias = torch.zeros(cfg.E, dtype=torch.float32, device=dev)
     out["bias_update"] = {"ms": timed(lambda: m.moe_bias_update(c, layer.counts, 1e-4, bias))}
