@@ -31,7 +31,7 @@ ERRORS = {
 EXPORTS = ("moe_validate_cfg", "moe_grouped_rows", "moe_workspace_bytes", "moe_workspace_init",
            "moe_pack_router", "moe_router_logits", "moe_route", "moe_permute", "moe_permute_noalloc",
            "moe_ep_layout", "moe_ep_layout_fp8", "moe_dispatch_recv_fp8", "moe_pack_w13",
-           "moe_grouped_ffn", "moe_grouped_ffn_gather", "moe_combine", "moe_bias_update", "moe_eplb_plan",
+           "moe_grouped_ffn", "moe_grouped_ffn_gather", "moe_grouped_ffn_train", "moe_combine", "moe_bias_update", "moe_eplb_plan",
            "moe_eplb_dispatch", "moe_pack_backward", "moe_combine_backward",
            "moe_backward_workspace_bytes", "moe_grouped_ffn_backward", "moe_permute_backward",
            "moe_get_device_status", "moe_strerror",
@@ -99,7 +99,9 @@ _sig = {
     "moe_combine_backward": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P]),
     "moe_backward_workspace_bytes": (_SZ, [_CFG]),
     "moe_grouped_ffn_backward": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
-                                                _P, _P, _P, _SZ, _P, _SZ, _P]),
+                                                _P, _P, _P, _P, _SZ, _P, _SZ, _P]),
+    "moe_grouped_ffn_train": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                             _P]),
     "moe_permute_backward": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
     "moe_get_device_status": (ctypes.c_int, [_P, _P]),
     "moe_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -271,15 +273,24 @@ def moe_backward_workspace_bytes(cfg) -> int:
     return _lib.moe_backward_workspace_bytes(ctypes.byref(cfg))
 
 
-def moe_grouped_ffn_backward(cfg, x_sorted, x, counts, offsets, W13, W13t, W2t, h, d_o, dx_sorted,
-                             dW13, dW2, bws, ws, stream=None):
+def moe_grouped_ffn_backward(cfg, x_sorted, x, counts, offsets, W13, W13t, W2t, h, g1, d_o,
+                             dx_sorted, dW13, dW2, bws, ws, stream=None):
     bp, bn = _ws(bws)
     p, n = _ws(ws)
     _check(_lib.moe_grouped_ffn_backward(ctypes.byref(cfg), _ptr(x_sorted), _ptr(x),
                                          _ptr(counts), _ptr(offsets), _ptr(W13), _ptr(W13t),
-                                         _ptr(W2t), _ptr(h), _ptr(d_o), _ptr(dx_sorted),
-                                         _ptr(dW13), _ptr(dW2), bp, bn, p, n, _stream(stream)),
-           "moe_grouped_ffn_backward")
+                                         _ptr(W2t), _ptr(h), _ptr(g1), _ptr(d_o),
+                                         _ptr(dx_sorted), _ptr(dW13), _ptr(dW2), bp, bn, p, n,
+                                         _stream(stream)), "moe_grouped_ffn_backward")
+
+
+def moe_grouped_ffn_train(cfg, x_sorted, x, counts, offsets, W13, W2, h, y_sorted, g1, ws,
+                          stream=None):
+    p, n = _ws(ws)
+    _check(_lib.moe_grouped_ffn_train(ctypes.byref(cfg), _ptr(x_sorted), _ptr(x), _ptr(counts),
+                                      _ptr(offsets), _ptr(W13), _ptr(W2), _ptr(h),
+                                      _ptr(y_sorted), _ptr(g1), p, n, _stream(stream)),
+           "moe_grouped_ffn_train")
 
 
 def moe_permute_backward(cfg, dx_sorted, inv, dx, stream=None):

@@ -101,28 +101,40 @@ __global__ void __launch_bounds__(32) kpad_offsets_kernel(const int32_t* __restr
 // ---------------------------------------------------------------------------
 constexpr int kTr = 64;
 
-// One 64 x 64 tile: src rows [r0, r0 + 64) (row i valid when i < n_valid, else
-// zero), columns [c0, c0 + 64) -> dst row c, columns [dc0, dc0 + 64).
+// One 64 x 64 tile: src rows [0, 64) (row i valid when i < n_valid, else
+// zero), columns [c0, c0 + 64) -> dst row c0 + c, columns [dc0, dc0 + 64).
+// The tile sits in shared memory as 32-bit words, 33 per row (one spare word
+// spreads a column's rows over the banks); each thread then writes two
+// destination rows (a pair of source columns) of 8 elements each.
 __device__ __forceinline__ void transpose_tile(const __nv_bfloat16* __restrict__ src, size_t ld_src,
                                                int n_valid, int c0, __nv_bfloat16* __restrict__ dst,
-                                               size_t ld_dst, size_t dc0,
-                                               __nv_bfloat16 (*tile)[kTr + 8]) {
-  // load: 64 rows x 128 bytes = 512 vectors of 8 elements, 2 per thread
+                                               size_t ld_dst, size_t dc0, uint32_t* tile) {
+  constexpr int P = kTr / 2 + 1;  // words per tile row
   for (int i = threadIdx.x; i < kTr * (kTr / 8); i += blockDim.x) {
     const int r = i / (kTr / 8), cv = i % (kTr / 8);
     uint4 v = make_uint4(0, 0, 0, 0);
     if (r < n_valid) v = __ldg(reinterpret_cast<const uint4*>(src + size_t(r) * ld_src + c0) + cv);
-    *reinterpret_cast<uint4*>(&tile[r][cv * 8]) = v;
+    uint32_t* w = tile + r * P + cv * 4;
+    w[0] = v.x;
+    w[1] = v.y;
+    w[2] = v.z;
+    w[3] = v.w;
   }
   __syncthreads();
-  // store: dst row c takes column c of the tile, 8 elements per vector
-  for (int i = threadIdx.x; i < kTr * (kTr / 8); i += blockDim.x) {
-    const int c = i / (kTr / 8), rv = i % (kTr / 8);
-    __align__(16) __nv_bfloat16 e[8];
+  for (int i = threadIdx.x; i < (kTr / 2) * (kTr / 8); i += blockDim.x) {
+    const int rv = i % (kTr / 8), c2 = i / (kTr / 8);  // rows 8rv..8rv+7, columns 2c2, 2c2+1
+    uint32_t lo[4], hi[4];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) e[q] = tile[rv * 8 + q][c];
-    *reinterpret_cast<uint4*>(dst + size_t(c0 + c) * ld_dst + dc0 + rv * 8) =
-        *reinterpret_cast<const uint4*>(e);
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t a = tile[(rv * 8 + 2 * q) * P + c2];
+      const uint32_t b = tile[(rv * 8 + 2 * q + 1) * P + c2];
+      lo[q] = (a & 0xffffu) | (b << 16);          // column 2c2 of rows 2q, 2q+1
+      hi[q] = (a >> 16) | (b & 0xffff0000u);      // column 2c2+1
+    }
+    *reinterpret_cast<uint4*>(dst + size_t(c0 + 2 * c2) * ld_dst + dc0 + rv * 8) =
+        make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    *reinterpret_cast<uint4*>(dst + size_t(c0 + 2 * c2 + 1) * ld_dst + dc0 + rv * 8) =
+        make_uint4(hi[0], hi[1], hi[2], hi[3]);
   }
   __syncthreads();
 }
@@ -137,7 +149,7 @@ __global__ void __launch_bounds__(256) transpose_segments_kernel(
     const int32_t* __restrict__ offsets, const int32_t* __restrict__ counts, int capacity, int E,
     int has_shared, int T, const int32_t* __restrict__ kpad_off, __nv_bfloat16* __restrict__ dst,
     size_t ld_dst) {
-  __shared__ __align__(16) __nv_bfloat16 tile[kTr][kTr + 8];
+  __shared__ uint32_t tile[kTr * (kTr / 2 + 1)];
   const int n = E + has_shared;
   const int col = blockIdx.x * kTr;
   if (col >= __ldg(kpad_off + n)) return;
@@ -167,7 +179,7 @@ __global__ void __launch_bounds__(256) transpose_segments_kernel(
 __global__ void __launch_bounds__(256) transpose_batched_kernel(const __nv_bfloat16* __restrict__ src,
                                                                 int rows, int cols,
                                                                 __nv_bfloat16* __restrict__ dst) {
-  __shared__ __align__(16) __nv_bfloat16 tile[kTr][kTr + 8];
+  __shared__ uint32_t tile[kTr * (kTr / 2 + 1)];
   const size_t mat = size_t(rows) * cols * blockIdx.z;
   const int r0 = blockIdx.y * kTr, c0 = blockIdx.x * kTr;
   transpose_tile(src + mat + size_t(r0) * cols, cols, kTr, c0, dst + mat, rows, size_t(r0), tile);

@@ -41,7 +41,8 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr int MAX_SEG = 1025;
 constexpr uint64_t WAIT_NS = 1000000000ull;
 constexpr uint64_t DRAIN_NS = 100000000ull;
-constexpr size_t DYN_SMEM = size_t(STAGES) * STAGE_BYTES + 1024;
+constexpr uint32_t EPI_STAGE_BYTES = 32 * 128;  // per epilogue warp: 32 rows x 64 bf16
+constexpr size_t DYN_SMEM = size_t(STAGES) * STAGE_BYTES + 4 * EPI_STAGE_BYTES + 1024;
 }  // namespace gg
 
 enum { kEpiSwiglu = 0, kEpiBf16 = 1, kEpiF32 = 2, kEpiSwigluBwd = 3 };
@@ -79,6 +80,12 @@ struct GroupedParams {
   // shared by all segments; zero-padded to multiples of 64 per segment).
   const int32_t* kpad_off;
   int m_out;
+  // kEpiBf16: 1 = groups of 32 rows whose rows are all valid leave through a
+  // tensor store of tmOut (box 64 columns x 32 rows, 128-byte swizzle)
+  int tma_store;
+  // kEpiSwiglu: non-null = also keep the pre-activations, aux_out[:, n_blk*BN + c]
+  // = bf16(acc[:, c]) (gate and up columns packed like W13), ld_aux
+  __nv_bfloat16* aux_out;
 };
 
 struct GroupedCtl {
@@ -139,7 +146,8 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
                         const __grid_constant__ CUtensorMap tmA_sh,
                         const __grid_constant__ CUtensorMap tmA64,
                         const __grid_constant__ CUtensorMap tmA_sh64,
-                        const __grid_constant__ CUtensorMap tmB, const GroupedParams p) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmOut, const GroupedParams p) {
   using namespace gg;
   extern __shared__ uint8_t dyn_smem[];
   __shared__ GroupedCtl ctl;
@@ -219,6 +227,7 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
     tma_prefetch_desc(&tmA64);
     tma_prefetch_desc(&tmA_sh64);
     tma_prefetch_desc(&tmB);
+    if (p.tma_store) tma_prefetch_desc(&tmOut);
   }
   tc_fence_before();
   __syncthreads();
@@ -472,6 +481,22 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
           tmem_ld32(taddr + c, gv);
           tmem_ld32(taddr + BN / 2 + c, uv);
           tmem_ld_wait();
+          if (valid && p.aux_out) {
+            __nv_bfloat16* arow = p.aux_out + size_t(out_row0 + r) * p.ld_aux + n_blk * BN + c;
+            uint4* ug = reinterpret_cast<uint4*>(arow);
+            uint4* vg = reinterpret_cast<uint4*>(arow + BN / 2);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              ug[q] = make_uint4(pack_bf16x2(__uint_as_float(gv[8 * q]), __uint_as_float(gv[8 * q + 1])),
+                                 pack_bf16x2(__uint_as_float(gv[8 * q + 2]), __uint_as_float(gv[8 * q + 3])),
+                                 pack_bf16x2(__uint_as_float(gv[8 * q + 4]), __uint_as_float(gv[8 * q + 5])),
+                                 pack_bf16x2(__uint_as_float(gv[8 * q + 6]), __uint_as_float(gv[8 * q + 7])));
+              vg[q] = make_uint4(pack_bf16x2(__uint_as_float(uv[8 * q]), __uint_as_float(uv[8 * q + 1])),
+                                 pack_bf16x2(__uint_as_float(uv[8 * q + 2]), __uint_as_float(uv[8 * q + 3])),
+                                 pack_bf16x2(__uint_as_float(uv[8 * q + 4]), __uint_as_float(uv[8 * q + 5])),
+                                 pack_bf16x2(__uint_as_float(uv[8 * q + 6]), __uint_as_float(uv[8 * q + 7])));
+            }
+          }
           if (valid) {
             uint32_t packed[16];
 #pragma unroll
@@ -486,6 +511,37 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+          }
+        }
+      } else if (p.tma_store && !half && m_blk * BM + quarter * 32 + 31 < rows) {
+        // all 32 rows of this warp are valid: stage 64 columns at a time in
+        // shared memory (128-byte swizzle) and store them with one tensor copy
+        const int col0 = n_blk * BN;
+        uint8_t* stg = smem + STAGES * STAGE_BYTES + quarter * EPI_STAGE_BYTES;
+        const int out_r = out_row0 + m_blk * BM + quarter * 32;
+#pragma unroll 1
+        for (int c = 0; c < BN && col0 + c < p.N; c += 64) {
+          uint32_t v0[32], v1[32];
+          tmem_ld32(taddr + c, v0);
+          tmem_ld32(taddr + c + 32, v1);
+          if (lane == 0) bulk_wait_group_read0();  // the previous store has read the buffer
+          __syncwarp();
+          tmem_ld_wait();
+          uint8_t* row = stg + lane * 128;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t* src = q < 4 ? v0 + 8 * q : v1 + 8 * (q - 4);
+            const uint4 w = make_uint4(pack_bf16x2(__uint_as_float(src[0]), __uint_as_float(src[1])),
+                                       pack_bf16x2(__uint_as_float(src[2]), __uint_as_float(src[3])),
+                                       pack_bf16x2(__uint_as_float(src[4]), __uint_as_float(src[5])),
+                                       pack_bf16x2(__uint_as_float(src[6]), __uint_as_float(src[7])));
+            *reinterpret_cast<uint4*>(row + ((q ^ (lane & 7)) << 4)) = w;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmOut, stg, col0 + c, out_r);
+            bulk_commit_group();
           }
         }
       } else {
@@ -512,6 +568,7 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (p.tma_store && lane == 0) bulk_wait_group0();  // stores complete before the CTA ends
   }
 
   tc_fence_before();
@@ -592,11 +649,11 @@ static int set_smem_attr() {
 // bound on its tiles (rows_ub rows over at most n_seg segments).
 static int launch_gg(int64_t rows_ub, int n_seg, const CUtensorMap& a, const CUtensorMap& a_sh,
                      const CUtensorMap& a64, const CUtensorMap& a_sh64, const CUtensorMap& b,
-                     const GroupedParams& p, cudaStream_t st) {
+                     const CUtensorMap& out, const GroupedParams& p, cudaStream_t st) {
   const int sms = device_sm_count();
   const long long tiles = (rows_ub / gg::BM + n_seg) * ((p.N + gg::BN - 1) / gg::BN);
   const int grid = int(tiles < sms ? tiles : sms);
-  grouped_gemm_kernel<<<grid, gg::THREADS, gg::DYN_SMEM, st>>>(a, a_sh, a64, a_sh64, b, p);
+  grouped_gemm_kernel<<<grid, gg::THREADS, gg::DYN_SMEM, st>>>(a, a_sh, a64, a_sh64, b, out, p);
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_E_CUDA;
 }
@@ -648,7 +705,7 @@ int launch_router_tc(const moe_cfg& c, const void* x, const void* W_split, const
   p.status = status;
   const long long tiles = (long long)((c.T + BM - 1) / BM) * ((c.E + BN - 1) / BN);
   const int grid = int(tiles < sms ? tiles : sms);
-  grouped_gemm_kernel<<<grid, THREADS, DYN_SMEM, st>>>(mA, mA, mA64, mA64, mB, p);
+  grouped_gemm_kernel<<<grid, THREADS, DYN_SMEM, st>>>(mA, mA, mA64, mA64, mB, mB, p);
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_E_CUDA;
 }
@@ -684,8 +741,8 @@ int launch_pack_router(const moe_cfg& c, const float* W, void* out, cudaStream_t
 
 int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
                        const int32_t* gather_order, const int32_t* counts, const int32_t* offsets,
-                       const void* W13, const void* W2, void* h, void* y_sorted, void* ws,
-                       cudaStream_t st) {
+                       const void* W13, const void* W2, void* h, void* y_sorted, void* g1,
+                       void* ws, cudaStream_t st) {
   using namespace gg;
   if (!get_encoder()) return MOE_E_CUDA;
   if (set_smem_attr() != MOE_OK) return MOE_E_CUDA;
@@ -737,12 +794,15 @@ int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
   p1.status = ws_ptr<int>(ws, L.status);
   p1.gather_order = gather_order;
   p1.gather_k = c.k;
+  p1.aux_out = static_cast<__nv_bfloat16*>(g1);
+  p1.ld_aux = 2 * c.f;
   const long long t1 = mt_ub * ((p1.N + BN - 1) / BN);
   const int grid1 = int(t1 < sms ? t1 : sms);
-  grouped_gemm_kernel<<<grid1, THREADS, DYN_SMEM, st>>>(mA1, mA1s, mA1h, mA1sh, mB1, p1);
+  grouped_gemm_kernel<<<grid1, THREADS, DYN_SMEM, st>>>(mA1, mA1s, mA1h, mA1sh, mB1, mB1, p1);
 
   GroupedParams p2 = p1;
   p2.gather_order = nullptr;
+  p2.aux_out = nullptr;
   p2.K = c.f;
   p2.N = c.d;
   p2.mode = kEpiBf16;
@@ -751,7 +811,10 @@ int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
   p2.ld_out = c.d;
   const long long t2 = mt_ub * ((p2.N + BN - 1) / BN);
   const int grid2 = int(t2 < sms ? t2 : sms);
-  grouped_gemm_kernel<<<grid2, THREADS, DYN_SMEM, st>>>(mA2, mA2, mA2h, mA2h, mB2, p2);
+  CUtensorMap mOut2;
+  if (!make_map(&mOut2, y_sorted, rows_h, c.d, 32)) return MOE_E_CUDA;
+  p2.tma_store = 1;
+  grouped_gemm_kernel<<<grid2, THREADS, DYN_SMEM, st>>>(mA2, mA2, mA2h, mA2h, mB2, mOut2, p2);
   note_launches(2);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_E_CUDA;
 }
@@ -789,7 +852,7 @@ BwdLayout backward_layout(const moe_cfg& c) {
 
 int launch_grouped_ffn_backward(const moe_cfg& c, const void* x_sorted, const void* x,
                                 const int32_t* counts, const int32_t* offsets, const void* W13,
-                                const void* W13t, const void* W2t, const void* h,
+                                const void* W13t, const void* W2t, const void* h, const void* g1_saved,
                                 const void* d_o, void* dx_sorted, void* dW13, void* dW2,
                                 void* bws, void* ws, cudaStream_t st) {
   using namespace gg;
@@ -801,7 +864,8 @@ int launch_grouped_ffn_backward(const moe_cfg& c, const void* x_sorted, const vo
   const int n_exp = c.E + c.has_shared;
   const uint64_t rows_h = uint64_t(R) + (c.has_shared ? c.T : 0);
   char* bw = static_cast<char*>(bws);
-  __nv_bfloat16* g1 = reinterpret_cast<__nv_bfloat16*>(bw + B.g1);
+  const __nv_bfloat16* g1 = g1_saved ? static_cast<const __nv_bfloat16*>(g1_saved)
+                                     : reinterpret_cast<const __nv_bfloat16*>(bw + B.g1);
   __nv_bfloat16* dg1 = reinterpret_cast<__nv_bfloat16*>(bw + B.dg1);
   int32_t* kpad = reinterpret_cast<int32_t*>(bw + B.kpad);
   __nv_bfloat16* trA = reinterpret_cast<__nv_bfloat16*>(bw + B.tr);
@@ -818,8 +882,9 @@ int launch_grouped_ffn_backward(const moe_cfg& c, const void* x_sorted, const vo
   base.k_passes = 1;
   base.status = ws_ptr<int>(ws, L.status);
 
-  // 1. g1 = x W13^T (recomputed; routed rows from x_sorted, shared rows from x)
-  {
+  // 1. g1 = x W13^T (recomputed unless the forward kept it; routed rows from
+  //    x_sorted, shared rows from x)
+  if (!g1_saved) {
     CUtensorMap mA, mAh, mAs, mAsh, mB;
     const bool sx = c.has_shared;
     if (!make_map(&mA, x_sorted, uint64_t(R), c.d, BM)) return MOE_E_CUDA;
@@ -834,9 +899,13 @@ int launch_grouped_ffn_backward(const moe_cfg& c, const void* x_sorted, const vo
     p.N = 2 * c.f;
     p.mode = kEpiBf16;
     p.shared_a_separate = 1;
-    p.out = g1;
+    __nv_bfloat16* g1w = reinterpret_cast<__nv_bfloat16*>(bw + B.g1);
+    p.out = g1w;
     p.ld_out = 2 * c.f;
-    MOE_TRY_INTERNAL(launch_gg(rows_h, n_exp, mA, mAs, mAh, mAsh, mB, p, st));
+    CUtensorMap mO;
+    if (!make_map(&mO, g1w, rows_h, 2 * c.f, 32)) return MOE_E_CUDA;
+    p.tma_store = 1;
+    MOE_TRY_INTERNAL(launch_gg(rows_h, n_exp, mA, mAs, mAh, mAsh, mB, mO, p, st));
   }
   // 2. dh = d_o W2 (B = W2^T per expert, N = f, K = d); the epilogue applies the
   //    SwiGLU derivative with g1 and writes dg1 (packed like W13)
@@ -854,7 +923,7 @@ int launch_grouped_ffn_backward(const moe_cfg& c, const void* x_sorted, const vo
     p.ld_aux = 2 * c.f;
     p.out = dg1;
     p.ld_out = 2 * c.f;
-    MOE_TRY_INTERNAL(launch_gg(rows_h, n_exp, mA, mA, mAh, mAh, mB, p, st));
+    MOE_TRY_INTERNAL(launch_gg(rows_h, n_exp, mA, mA, mAh, mAh, mB, mB, p, st));
   }
   // 3. dx_sorted = dg1 W13 (B = W13^T per expert, N = d, K = 2f)
   {
@@ -869,7 +938,10 @@ int launch_grouped_ffn_backward(const moe_cfg& c, const void* x_sorted, const vo
     p.shared_a_separate = 0;
     p.out = static_cast<__nv_bfloat16*>(dx_sorted);
     p.ld_out = c.d;
-    MOE_TRY_INTERNAL(launch_gg(rows_h, n_exp, mA, mA, mAh, mAh, mB, p, st));
+    CUtensorMap mO;
+    if (!make_map(&mO, dx_sorted, rows_h, c.d, 32)) return MOE_E_CUDA;
+    p.tma_store = 1;
+    MOE_TRY_INTERNAL(launch_gg(rows_h, n_exp, mA, mA, mAh, mAh, mB, mO, p, st));
   }
   // 4. weight gradients, each over its expert's rows
   MOE_TRY_INTERNAL(launch_kpad_offsets(c, counts, kpad, st));
@@ -894,7 +966,10 @@ int launch_grouped_ffn_backward(const moe_cfg& c, const void* x_sorted, const vo
     p.m_out = c.d;
     p.out = static_cast<__nv_bfloat16*>(dW2);
     p.ld_out = c.f;
-    MOE_TRY_INTERNAL(launch_gg(int64_t(n_exp) * c.d, n_exp, mA, mA, mAh, mAh, mB, p, st));
+    CUtensorMap mO;
+    if (!make_map(&mO, dW2, uint64_t(n_exp) * c.d, c.f, 32)) return MOE_E_CUDA;
+    p.tma_store = 1;
+    MOE_TRY_INTERNAL(launch_gg(int64_t(n_exp) * c.d, n_exp, mA, mA, mAh, mAh, mB, mO, p, st));
   }
   __nv_bfloat16* trC = trA + size_t(2 * c.f) * kub;  // after dg1^T [2f, kub]
   MOE_TRY_INTERNAL(launch_transpose_segments(c, dg1, dg1 + size_t(R) * 2 * c.f, 2 * c.f, offsets,
@@ -915,7 +990,11 @@ int launch_grouped_ffn_backward(const moe_cfg& c, const void* x_sorted, const vo
     p.m_out = 2 * c.f;
     p.out = static_cast<__nv_bfloat16*>(dW13);
     p.ld_out = c.d;
-    MOE_TRY_INTERNAL(launch_gg(int64_t(n_exp) * 2 * c.f, n_exp, mA, mA, mAh, mAh, mB, p, st));
+    CUtensorMap mO;
+    if (!make_map(&mO, dW13, uint64_t(n_exp) * 2 * c.f, c.d, 32)) return MOE_E_CUDA;
+    p.tma_store = 1;
+    MOE_TRY_INTERNAL(launch_gg(int64_t(n_exp) * 2 * c.f, n_exp, mA, mA, mAh, mAh, mB, mO, p,
+                               st));
   }
   return MOE_OK;
 }

@@ -32,8 +32,8 @@ int launch_ep_layout(const moe_cfg& c, const int32_t* idx, const int32_t* offset
 int launch_pack_w13(const moe_cfg& c, const void* W1, const void* W3, void* W13, cudaStream_t st);
 int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
                        const int32_t* gather_order, const int32_t* counts, const int32_t* offsets,
-                       const void* W13, const void* W2, void* h, void* y_sorted, void* ws,
-                       cudaStream_t st);
+                       const void* W13, const void* W2, void* h, void* y_sorted, void* g1,
+                       void* ws, cudaStream_t st);
 int launch_combine(const moe_cfg& c, const void* y_sorted, const int32_t* inv, const float* gate,
                    void* y, cudaStream_t st);
 
@@ -68,8 +68,8 @@ int launch_transpose_segments(const moe_cfg& c, const void* src, const void* src
 int launch_grouped_ffn_backward(const moe_cfg& c, const void* x_sorted, const void* x,
                                 const int32_t* counts, const int32_t* offsets, const void* W13,
                                 const void* W13t, const void* W2t, const void* h,
-                                const void* d_o, void* dx_sorted, void* dW13, void* dW2,
-                                void* bws, void* ws, cudaStream_t st);
+                                const void* g1_saved, const void* d_o, void* dx_sorted,
+                                void* dW13, void* dW2, void* bws, void* ws, cudaStream_t st);
 
 // Row move shared by the permute and the send-buffer fill: for each token t
 // and slot j, copy x[t] to dst[rows[t*k + j]] when that row is >= 0.

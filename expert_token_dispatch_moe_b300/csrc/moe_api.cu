@@ -249,7 +249,8 @@ MOE_API int moe_grouped_ffn(const moe_cfg* c, const moe_bf16* x_sorted, const mo
   else MOE_TRY(check_opt({x}));
   MOE_TRY(check_ws(c, ws, ws_bytes));
   MOE_TRY(device_ok());
-  return launch_grouped_ffn(*c, x_sorted, x, nullptr, counts, offsets, W13, W2, h, y_sorted, ws,
+  return launch_grouped_ffn(*c, x_sorted, x, nullptr, counts, offsets, W13, W2, h, y_sorted,
+                            nullptr, ws,
                             static_cast<cudaStream_t>(stream));
 }
 
@@ -264,8 +265,26 @@ MOE_API int moe_grouped_ffn_gather(const moe_cfg* c, const moe_bf16* x, const in
   MOE_TRY(check_ptrs({x, order, counts, offsets, W13, W2, h, y_sorted}));
   MOE_TRY(check_ws(c, ws, ws_bytes));
   MOE_TRY(device_ok());
-  return launch_grouped_ffn(*c, nullptr, x, order, counts, offsets, W13, W2, h, y_sorted, ws,
-                            static_cast<cudaStream_t>(stream));
+  return launch_grouped_ffn(*c, nullptr, x, order, counts, offsets, W13, W2, h, y_sorted, nullptr,
+                            ws, static_cast<cudaStream_t>(stream));
+}
+
+MOE_API int moe_grouped_ffn_train(const moe_cfg* c, const moe_bf16* x_sorted, const moe_bf16* x,
+                                  const int32_t* counts, const int32_t* offsets,
+                                  const moe_bf16* W13, const moe_bf16* W2, moe_bf16* h,
+                                  moe_bf16* y_sorted, moe_bf16* g1, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  reset_launches();
+  MOE_TRY(moe_validate_cfg(c));
+  if (c->f < 128 || c->f % 128) return MOE_E_SHAPE;
+  if (c->E + c->has_shared > 1025) return MOE_E_SHAPE;
+  MOE_TRY(check_ptrs({x_sorted, counts, offsets, W13, W2, h, y_sorted, g1}));
+  if (c->has_shared) MOE_TRY(check_ptrs({x}));
+  else MOE_TRY(check_opt({x}));
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  MOE_TRY(device_ok());
+  return launch_grouped_ffn(*c, x_sorted, x, nullptr, counts, offsets, W13, W2, h, y_sorted, g1,
+                            ws, static_cast<cudaStream_t>(stream));
 }
 
 MOE_API int moe_combine(const moe_cfg* c, const moe_bf16* y_sorted, const int32_t* inv,
@@ -343,7 +362,8 @@ MOE_API int moe_grouped_ffn_backward(const moe_cfg* c, const moe_bf16* x_sorted,
                                      const int32_t* counts, const int32_t* offsets,
                                      const moe_bf16* W13, const moe_bf16* W13t,
                                      const moe_bf16* W2t, const moe_bf16* h,
-                                     const moe_bf16* d_o, moe_bf16* dx_sorted, moe_bf16* dW13,
+                                     const moe_bf16* g1, const moe_bf16* d_o,
+                                     moe_bf16* dx_sorted, moe_bf16* dW13,
                                      moe_bf16* dW2, void* bws, size_t bws_bytes, void* ws,
                                      size_t ws_bytes, void* stream) {
   reset_launches();
@@ -351,6 +371,7 @@ MOE_API int moe_grouped_ffn_backward(const moe_cfg* c, const moe_bf16* x_sorted,
   if (c->f < 128 || c->f % 128) return MOE_E_SHAPE;
   if (c->E + c->has_shared > 1025) return MOE_E_SHAPE;
   MOE_TRY(check_ptrs({x_sorted, counts, offsets, W13, W13t, W2t, h, d_o, dx_sorted, dW13, dW2}));
+  MOE_TRY(check_opt({g1}));
   if (c->has_shared) MOE_TRY(check_ptrs({x}));
   else MOE_TRY(check_opt({x}));
   if (!bws) return MOE_E_WORKSPACE;
@@ -358,7 +379,7 @@ MOE_API int moe_grouped_ffn_backward(const moe_cfg* c, const moe_bf16* x_sorted,
   if (bws_bytes < backward_layout(*c).total) return MOE_E_WORKSPACE;
   MOE_TRY(check_ws(c, ws, ws_bytes));
   MOE_TRY(device_ok());
-  return launch_grouped_ffn_backward(*c, x_sorted, x, counts, offsets, W13, W13t, W2t, h, d_o,
+  return launch_grouped_ffn_backward(*c, x_sorted, x, counts, offsets, W13, W13t, W2t, h, g1, d_o,
                                      dx_sorted, dW13, dW2, bws, ws,
                                      static_cast<cudaStream_t>(stream));
 }

@@ -16,6 +16,7 @@ import torch
 
 from . import (MoeCfg, moe_backward_workspace_bytes, moe_combine, moe_combine_backward,
                moe_ep_layout, moe_grouped_ffn, moe_grouped_ffn_backward, moe_grouped_ffn_gather,
+               moe_grouped_ffn_train,
                moe_grouped_rows, moe_last_launch_count, moe_pack_backward, moe_pack_router,
                moe_pack_w13, moe_permute, moe_permute_backward, moe_route, moe_router_logits,
                moe_workspace_bytes, moe_workspace_init)
@@ -28,9 +29,11 @@ TC_ROUTER_MIN_E = 17
 
 class MoELayer:
     def __init__(self, cfg, W1, W3, W2, W_r=None, logit_bias=None, selection_bias=None,
-                 device=None, with_send_buf=True, tc_router=None, gather=False):
+                 device=None, with_send_buf=True, tc_router=None, gather=False, train=False):
         """gather=True: the permute computes indices only and GEMM 1 gathers its
-        rows from x (moe_grouped_ffn_gather); x_sorted is not written."""
+        rows from x (moe_grouped_ffn_gather); x_sorted is not written.
+        train=True: the forward keeps GEMM 1's pre-activations (self.g1) so the
+        backward need not recompute them."""
         self.cfg = cfg if isinstance(cfg, MoeCfg) else MoeCfg.from_layer(cfg)
         c = self.cfg
         dev = torch.device(device or "cuda")
@@ -72,6 +75,8 @@ class MoELayer:
         self.ws = torch.zeros(moe_workspace_bytes(c), dtype=torch.uint8, device=dev)
         moe_workspace_init(c, self.ws)
         self.gather = gather
+        self.train = train
+        self.g1 = torch.empty(rows, 2 * c.f, dtype=bf16, device=dev) if train else None
         self.launches_per_forward = None
         self.launches_per_backward = None
         self.W13t = None        # backward buffers, allocated on the first backward
@@ -104,6 +109,10 @@ class MoELayer:
         if self.gather:
             moe_grouped_ffn_gather(c, x, self.order, self.counts, self.offsets, self.W13, self.W2,
                                    self.h, self.y_sorted, self.ws)
+        elif self.train:
+            moe_grouped_ffn_train(c, self.x_sorted, x if c.has_shared else None, self.counts,
+                                  self.offsets, self.W13, self.W2, self.h, self.y_sorted, self.g1,
+                                  self.ws)
         else:
             moe_grouped_ffn(c, self.x_sorted, x if c.has_shared else None, self.counts,
                             self.offsets, self.W13, self.W2, self.h, self.y_sorted, self.ws)
@@ -142,8 +151,8 @@ class MoELayer:
         moe_combine_backward(c, dy, self.y_sorted, self.inv, self.topk_gate, self.d_o, self.dgate)
         n = moe_last_launch_count()
         moe_grouped_ffn_backward(c, self.x_sorted, x if c.has_shared else None, self.counts,
-                                 self.offsets, self.W13, self.W13t, self.W2t, self.h, self.d_o,
-                                 self.dx_sorted, self.dW13, self.dW2, self.bws, self.ws)
+                                 self.offsets, self.W13, self.W13t, self.W2t, self.h, self.g1,
+                                 self.d_o, self.dx_sorted, self.dW13, self.dW2, self.bws, self.ws)
         n += moe_last_launch_count()
         moe_permute_backward(c, self.dx_sorted, self.inv, self.dx)
         n += moe_last_launch_count()

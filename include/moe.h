@@ -317,8 +317,20 @@ int moe_combine_backward(const moe_cfg* cfg, const moe_bf16* dy, const moe_bf16*
  * invalid configuration).  Host only. */
 size_t moe_backward_workspace_bytes(const moe_cfg* cfg);
 
+/* Step 5 for training: moe_grouped_ffn that also keeps GEMM 1's output before
+ * the SwiGLU, for moe_grouped_ffn_backward (which then need not recompute it).
+ *   g1  bf16 [R + has_shared*T, 2f] out: x W13^T rounded to bf16, columns packed
+ *       like W13 rows (each 256-column block: 128 gate then 128 up columns);
+ *       rows of the kept assignments and the shared expert
+ *   other arguments and outputs as for moe_grouped_ffn. */
+int moe_grouped_ffn_train(const moe_cfg* cfg, const moe_bf16* x_sorted, const moe_bf16* x,
+                          const int32_t* counts, const int32_t* offsets, const moe_bf16* W13,
+                          const moe_bf16* W2, moe_bf16* h, moe_bf16* y_sorted, moe_bf16* g1,
+                          void* ws, size_t ws_bytes, void* stream);
+
 /* Step 5 backward, on the tensor cores:
- *   g1 = x W13^T (recomputed into the backward workspace),
+ *   g1 = x W13^T (the forward's, from moe_grouped_ffn_train, or recomputed into
+ *        the backward workspace when g1 is NULL),
  *   dg1 = SwiGLU'(g1) applied to d_o W2 (fused into that product's epilogue;
  *         du = dh v s (1 + u (1 - s)), dv = dh u s, s = sigmoid(u)),
  *   dx_sorted = dg1 W13,
@@ -326,8 +338,8 @@ size_t moe_backward_workspace_bytes(const moe_cfg* cfg);
  *   operands transposed into the workspace, each expert's rows starting on a
  *   64-column boundary, zero-padded).
  *   x_sorted, x, counts, offsets, W13 as for moe_grouped_ffn; W13t, W2t from
- *   moe_pack_backward; h the forward's [R + has_shared*T, f]; d_o from
- *   moe_combine_backward.
+ *   moe_pack_backward; h the forward's [R + has_shared*T, f]; g1 from
+ *   moe_grouped_ffn_train or NULL; d_o from moe_combine_backward.
  *   dx_sorted bf16 [R + has_shared*T, d] out (kept and shared rows)
  *   dW13      bf16 [E + has_shared, 2f, d] out, rows packed like W13
  *   dW2       bf16 [E + has_shared, d, f] out (zero for an expert with no rows)
@@ -336,9 +348,9 @@ size_t moe_backward_workspace_bytes(const moe_cfg* cfg);
 int moe_grouped_ffn_backward(const moe_cfg* cfg, const moe_bf16* x_sorted, const moe_bf16* x,
                              const int32_t* counts, const int32_t* offsets,
                              const moe_bf16* W13, const moe_bf16* W13t, const moe_bf16* W2t,
-                             const moe_bf16* h, const moe_bf16* d_o, moe_bf16* dx_sorted,
-                             moe_bf16* dW13, moe_bf16* dW2, void* bws, size_t bws_bytes,
-                             void* ws, size_t ws_bytes, void* stream);
+                             const moe_bf16* h, const moe_bf16* g1, const moe_bf16* d_o,
+                             moe_bf16* dx_sorted, moe_bf16* dW13, moe_bf16* dW2, void* bws,
+                             size_t bws_bytes, void* ws, size_t ws_bytes, void* stream);
 
 /* Step 2 backward: the permute's gradient is a combine with unit gates,
  *   dx[t] = sum over kept j of dx_sorted[inv[t*k+j]] (+ dx_sorted[R + t] with a

@@ -134,3 +134,28 @@ def test_backward_full_size_sampled(m, name):
     _close(npf(dW1[e]), dW1r, "dW1[e]")
     _close(npf(dW3[e]), dW3r, "dW3[e]")
     _close(npf(layer.dW2[e]), dW2r, "dW2[e]")
+
+
+@pytest.mark.parametrize("name", ["ds_small", "skew_small", "tiny_ragged"])
+def test_backward_with_saved_preactivations_is_identical(m, name):
+    """The training forward keeps GEMM 1's output (g1); the backward that reads it
+    gives bit-identical gradients to the backward that recomputes it, and the
+    training forward's y is the inference forward's."""
+    cfg = SMALL[name]
+    x = synth.make_x(cfg, device="cuda")
+    scores = synth.make_scores(cfg, device="cuda")
+    if name == "skew_small":
+        scores[:, 0] += 4.5
+    W1, W3, W2 = synth.make_expert_weights(cfg, device="cuda")
+    dy = _dy(cfg, "cuda")
+    a = m.MoELayer(cfg, W1, W3, W2)
+    b = m.MoELayer(cfg, W1, W3, W2, train=True)
+    a.forward(x, scores=scores)
+    b.forward(x, scores=scores)
+    assert torch.equal(a.y.view(torch.int16), b.y.view(torch.int16))
+    a.backward(x, dy)
+    b.backward(x, dy)
+    torch.cuda.synchronize()
+    for name_ in ("dx", "dW13", "dW2"):
+        assert torch.equal(getattr(a, name_).view(torch.int16), getattr(b, name_).view(torch.int16)), name_
+    assert torch.equal(a.dgate, b.dgate)
