@@ -282,17 +282,43 @@ def _profiled_traffic(cfg):
     return None
 
 
-def _roofline(cfg, ffn_tflops, pk):
+def _ffn_bytes(cfg, counts_np):
+    """Algorithmic DRAM bytes of the two grouped GEMMs: the weights of every
+    expert that received rows (and the shared expert) once, A rows read once, h
+    written and read once, y_sorted written once."""
+    kept = np.minimum(counts_np, cfg.capacity) if cfg.capacity else counts_np
+    touched = int((kept > 0).sum()) + (1 if cfg.has_shared else 0)
+    rows = int(kept.sum()) + (cfg.T if cfg.has_shared else 0)
+    w = touched * 3 * cfg.d * cfg.f * 2
+    return w + rows * cfg.d * 2 * 2 + rows * cfg.f * 2 * 2
+
+
+def _roofline(cfg, ffn_ms, ffn_flops, ffn_bytes, pk):
     """The dominant kernel (both grouped GEMM launches of a step) against the
-    measured bf16 peak.  The kernel runs inside a loop of hundreds of steps under
-    the board power limit, so the sustained figure is the denominator; the burst
-    fraction is reported beside it."""
-    peak = pk["bf16_tflops_sustained"] or pk["bf16_tflops"]
-    return {"bound": "tensor", "kernel": "grouped_gemm_kernel (GEMM 1 + GEMM 2 of one step)",
-            "achieved": ffn_tflops, "peak": peak, "unit": "TFLOP/s", "frac": ffn_tflops / peak,
-            "peak_source": pk["source"] + (" sustained" if pk["bf16_tflops_sustained"] else " burst"),
-            "frac_of_burst_peak": ffn_tflops / pk["bf16_tflops"],
-            "traffic": _profiled_traffic(cfg)}
+    roofline that bounds it: the measured bf16 peak when its FLOPs take longer
+    than its bytes at the measured copy bandwidth, else HBM.  The kernel runs
+    inside a loop of hundreds of steps under the board power limit, so the
+    sustained bf16 figure is the tensor denominator; the burst fraction is
+    reported beside it."""
+    peak_tf = pk["bf16_tflops_sustained"] or pk["bf16_tflops"]
+    t_flops = ffn_flops / (peak_tf * 1e12)
+    t_bytes = ffn_bytes / (pk["hbm_gbs"] * 1e9)
+    tflops = ffn_flops / (ffn_ms * 1e-3) / 1e12
+    base = {"kernel": "grouped_gemm_kernel (GEMM 1 + GEMM 2 of one step)",
+            "traffic": _profiled_traffic(cfg), "algorithmic_bytes": ffn_bytes,
+            "algorithmic_flops": ffn_flops}
+    if t_flops >= t_bytes:
+        base.update({"bound": "tensor", "achieved": tflops, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": tflops / peak_tf,
+                     "peak_source": pk["source"] + (" sustained" if pk["bf16_tflops_sustained"]
+                                                    else " burst"),
+                     "frac_of_burst_peak": tflops / pk["bf16_tflops"]})
+    else:
+        gbs = ffn_bytes / (ffn_ms * 1e-3) / 1e9
+        base.update({"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / pk["hbm_gbs"], "peak_source": pk["source"] + " copy",
+                     "tflops": tflops})
+    return base
 
 
 def run_ours(args, cfg):
@@ -436,7 +462,8 @@ def run_ours(args, cfg):
         "e2e": {"value": cfg.T * world / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 2},
         "gpu_launches": launches_per_step * args.steps,
-        "roofline": _roofline(cfg, ffn_tflops, pk),
+        "roofline": _roofline(cfg, kt["grouped_ffn"], alg["ffn_flops"], _ffn_bytes(cfg, counts),
+                              pk),
         "kernels": kernels,
         "wall_s": wall,
     }

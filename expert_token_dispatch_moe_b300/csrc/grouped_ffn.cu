@@ -83,6 +83,9 @@ struct GroupedParams {
   // kEpiBf16: 1 = groups of 32 rows whose rows are all valid leave through a
   // tensor store of tmOut (box 64 columns x 32 rows, 128-byte swizzle)
   int tma_store;
+  // MMA width (N of each tcgen05.mma and columns of a tile): 0 = BN.  A narrower
+  // width (a multiple of 16) serves outputs with few columns (the router).
+  int n_mma;
   // kEpiSwiglu: non-null = also keep the pre-activations, aux_out[:, n_blk*BN + c]
   // = bf16(acc[:, c]) (gate and up columns packed like W13), ld_aux
   __nv_bfloat16* aux_out;
@@ -155,7 +158,9 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
                                              ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_seg = p.counts ? p.E + p.has_shared : 1;
-  const int n_blocks_n = (p.N + BN - 1) / BN;
+  const int NM = p.n_mma ? p.n_mma : BN;                // tile width
+  const uint32_t b_bytes = uint32_t(NM) * BK * 2;
+  const int n_blocks_n = (p.N + NM - 1) / NM;
   const bool wgrad = p.kpad_off != nullptr;
   const int kb_per_pass = wgrad ? (1 << 30) : p.K / BK;
   const int num_kb = wgrad ? 0 : kb_per_pass * p.k_passes;
@@ -268,9 +273,9 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
           const bool sep = p.counts && g >= p.E && p.shared_a_separate;
           const bool half = is_half(rows, m_blk);
           const CUtensorMap* ma = half ? (sep ? &tmA_sh64 : &tmA64) : (sep ? &tmA_sh : &tmA);
-          const uint32_t tx = half ? A_BYTES / 2 + B_BYTES : STAGE_BYTES;
+          const uint32_t tx = (half ? A_BYTES / 2 : A_BYTES) + b_bytes;
           const int a_row = a_row0 + m_blk * BM;
-          const int b_row = (wgrad ? 0 : g * p.N) + n_blk * BN;
+          const int b_row = (wgrad ? 0 : g * p.N) + n_blk * NM;
           int k0, nkb;
           tile_k(g, k0, nkb);
           for (int kb = 0; kb < nkb; ++kb) {
@@ -306,9 +311,9 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
           }
         }
         const CUtensorMap* ma = half ? (sep ? &tmA_sh64 : &tmA64) : (sep ? &tmA_sh : &tmA);
-        const uint32_t tx = half ? A_BYTES / 2 + B_BYTES : STAGE_BYTES;
+        const uint32_t tx = (half ? A_BYTES / 2 : A_BYTES) + b_bytes;
         const int a_row = a_row0 + m_blk * BM;
-        const int b_row = g * p.N + n_blk * BN;
+        const int b_row = g * p.N + n_blk * NM;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (lane == 0) ok = wait_or_abort(&ctl.empty[stage], phase ^ 1u, ctl, p.status);
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -357,8 +362,8 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         int g, m_blk, n_blk, rows, a_row0, out_row0;
         decode(t, g, m_blk, n_blk, rows, a_row0, out_row0);
-        const uint32_t idesc = is_half(rows, m_blk) ? idesc_bf16_f32(BM / 2, BN)
-                                                    : idesc_bf16_f32(BM, BN);
+        const uint32_t idesc = is_half(rows, m_blk) ? idesc_bf16_f32(BM / 2, NM)
+                                                    : idesc_bf16_f32(BM, NM);
         int k0, nkb;
         tile_k(g, k0, nkb);
         if (!wait_or_abort(&ctl.acc_empty[acc], acc_phase ^ 1u, ctl, p.status)) break;
@@ -453,9 +458,9 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
           }
         }
       } else if (p.mode == kEpiF32) {
-        const int col0 = n_blk * BN;
+        const int col0 = n_blk * NM;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = 0; c < NM; c += 32) {
           uint32_t v[32];
           tmem_ld32(taddr + c, v);
           tmem_ld_wait();
@@ -497,16 +502,16 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
                                  pack_bf16x2(__uint_as_float(uv[8 * q + 6]), __uint_as_float(uv[8 * q + 7])));
             }
           }
-          if (valid) {
-            uint32_t packed[16];
+          uint32_t packed[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float g0 = __uint_as_float(gv[2 * i]), g1 = __uint_as_float(gv[2 * i + 1]);
-              const float u0 = __uint_as_float(uv[2 * i]), u1 = __uint_as_float(uv[2 * i + 1]);
-              const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
-              const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
-              packed[i] = pack_bf16x2(h0, h1);
-            }
+          for (int i = 0; i < 16; ++i) {
+            const float g0 = __uint_as_float(gv[2 * i]), g1 = __uint_as_float(gv[2 * i + 1]);
+            const float u0 = __uint_as_float(uv[2 * i]), u1 = __uint_as_float(uv[2 * i + 1]);
+            const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
+            const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
+            packed[i] = pack_bf16x2(h0, h1);
+          }
+          if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(orow + col0 + c);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -684,10 +689,12 @@ int launch_router_tc(const moe_cfg& c, const void* x, const void* W_split, const
   using namespace gg;
   if (!get_encoder()) return MOE_E_CUDA;
   if (set_smem_attr() != MOE_OK) return MOE_E_CUDA;
+  // MMA width: the experts rounded up to 16 (at most 256 per tile)
+  const int nm = c.E >= BN ? BN : ((c.E + 15) & ~15);
   CUtensorMap mA, mA64, mB;
   if (!make_map(&mA, x, uint64_t(c.T), c.d, BM)) return MOE_E_CUDA;
   if (!make_map(&mA64, x, uint64_t(c.T), c.d, BM / 2)) return MOE_E_CUDA;
-  if (!make_map(&mB, W_split, uint64_t(3) * c.E, c.d, BN)) return MOE_E_CUDA;
+  if (!make_map(&mB, W_split, uint64_t(3) * c.E, c.d, uint32_t(nm))) return MOE_E_CUDA;
   const int sms = sm_count();
   if (sms <= 0) return MOE_E_CUDA;
   GroupedParams p{};
@@ -703,6 +710,7 @@ int launch_router_tc(const moe_cfg& c, const void* x, const void* W_split, const
   p.sigmoid = c.score_fn == MOE_SIGMOID;
   p.ld_out = c.E;
   p.status = status;
+  p.n_mma = nm;
   const long long tiles = (long long)((c.T + BM - 1) / BM) * ((c.E + BN - 1) / BN);
   const int grid = int(tiles < sms ? tiles : sms);
   grouped_gemm_kernel<<<grid, THREADS, DYN_SMEM, st>>>(mA, mA, mA64, mA64, mB, mB, p);
@@ -796,6 +804,7 @@ int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
   p1.gather_k = c.k;
   p1.aux_out = static_cast<__nv_bfloat16*>(g1);
   p1.ld_aux = 2 * c.f;
+
   const long long t1 = mt_ub * ((p1.N + BN - 1) / BN);
   const int grid1 = int(t1 < sms ? t1 : sms);
   grouped_gemm_kernel<<<grid1, THREADS, DYN_SMEM, st>>>(mA1, mA1s, mA1h, mA1sh, mB1, mB1, p1);
