@@ -502,16 +502,19 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
                                  pack_bf16x2(__uint_as_float(uv[8 * q + 6]), __uint_as_float(uv[8 * q + 7])));
             }
           }
-          uint32_t packed[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float g0 = __uint_as_float(gv[2 * i]), g1 = __uint_as_float(gv[2 * i + 1]);
-            const float u0 = __uint_as_float(uv[2 * i]), u1 = __uint_as_float(uv[2 * i + 1]);
-            const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
-            const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
-            packed[i] = pack_bf16x2(h0, h1);
-          }
+          // only valid rows are activated: rows past the segment hold stale
+          // accumulators, and activating them anyway made GEMM 1 about 30 %
+          // slower on a capacity-padded layer
           if (valid) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float g0 = __uint_as_float(gv[2 * i]), g1 = __uint_as_float(gv[2 * i + 1]);
+              const float u0 = __uint_as_float(uv[2 * i]), u1 = __uint_as_float(uv[2 * i + 1]);
+              const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
+              const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
+              packed[i] = pack_bf16x2(h0, h1);
+            }
             uint4* dst = reinterpret_cast<uint4*>(orow + col0 + c);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
