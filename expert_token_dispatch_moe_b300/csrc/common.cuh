@@ -146,6 +146,17 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// Plain bulk copy of `bytes` contiguous bytes, global -> shared, completion on
+// an mbarrier (addresses 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load_1d(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                             uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Four rows r0..r3 (any order, any rows of the tensor) of a tensor map whose
 // box is one row high, columns [c0, c0 + box width), into consecutive rows of
 // shared memory at smem_dst (128-byte aligned; the swizzle pattern follows the

@@ -17,7 +17,7 @@ void note_launches(int n);
 int device_sm_count();
 
 int launch_router_logits(const moe_cfg& c, const void* x, const float* W, const float* lbias,
-                         float* out, cudaStream_t st);
+                         float* out, int* status, cudaStream_t st);
 int launch_router_tc(const moe_cfg& c, const void* x, const void* W_split, const float* lbias,
                      float* out, int* status, cudaStream_t st);
 int launch_pack_router(const moe_cfg& c, const float* W, void* out, cudaStream_t st);

@@ -150,11 +150,9 @@ MOE_API int moe_router_logits(const moe_cfg* c, const moe_bf16* x, const float* 
   if (ws) MOE_TRY(check_ws(c, ws, ws_bytes));
   MOE_TRY(device_ok());
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (W_r_split) {
-    int* status = ws ? ws_ptr<int>(ws, ws_layout(*c).status) : nullptr;
-    return launch_router_tc(*c, x, W_r_split, logit_bias, scores, status, st);
-  }
-  return launch_router_logits(*c, x, W_r, logit_bias, scores, st);
+  int* status = ws ? ws_ptr<int>(ws, ws_layout(*c).status) : nullptr;
+  if (W_r_split) return launch_router_tc(*c, x, W_r_split, logit_bias, scores, status, st);
+  return launch_router_logits(*c, x, W_r, logit_bias, scores, status, st);
 }
 
 MOE_API int moe_route(const moe_cfg* c, const float* scores, const float* bias, int32_t* topk_idx,

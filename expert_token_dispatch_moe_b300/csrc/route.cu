@@ -6,6 +6,8 @@
 //   order (value desc, expert asc), optional selection bias and group-limited
 //   (node-limited) pre-selection ("What DeepSeek-V3 did about it"), then
 //   softmax or (normalised) sigmoid gates.
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -172,88 +174,215 @@ __global__ void __launch_bounds__(256) route_topk_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// Router logits, E <= 16: each warp handles 4 tokens; W_r is staged through
-// shared memory in pieces of 1024 rows (rows padded so that the 8 rows a lane
-// reads start on distinct banks).
+// Router logits, E <= 16, fp32 SIMT.  Every lane keeps a COLS x EP block of W_r
+// in registers (COLS = 64 / EP columns of d: column pairs 2L, 2L + 1 of each
+// 64-column group of its warp, so that the warp's loads of W_r rows and its
+// shared-memory reads of x are both contiguous); a warp covers 32 * COLS
+// columns and a block of kRlWarps warps a column tile of 512 * COLS (4096
+// columns at EP = 8).  The block's tokens stream through a
+// ring of shared-memory stages filled by bulk copies (TB = 32 / EP token rows
+// of one column tile per stage, 128 KB in flight), so the loads of later
+// tokens overlap the arithmetic of earlier ones.  Per stage a lane holds
+// TB * EP = 32 partial sums; a butterfly transpose-reduce over the warp (31
+// shuffles) leaves lane L with the warp's sum for token L / EP, expert L % EP.
+// Warp sums accumulate in shared memory, one slot per warp; the block adds the
+// warps in index order at the end, so the result does not depend on timing.
+// Waits are bounded (1 s): on time-out the block records
+// MOE_E_DEVICE_TIMEOUT (when given a status word), drains its copies and
+// writes nothing.
 // ---------------------------------------------------------------------------
-constexpr int kRlTok = 4;       // tokens per warp
-constexpr int kRlPiece = 1024;  // W_r rows per shared-memory piece
+constexpr int kRlWarps = 16;
+constexpr int kRlMaxTok = 64;               // tokens per block at most
+constexpr uint32_t kRlRingBytes = 128 * 1024;
+constexpr uint64_t kRlWaitNs = 1000000000ull;
+constexpr uint64_t kRlDrainNs = 100000000ull;
 
 template <int EP>
-__global__ void __launch_bounds__(256) router_logits_small_kernel(
-    const __nv_bfloat16* __restrict__ x, const float* __restrict__ W, const float* __restrict__ lbias,
-    int T, int d, int E, int score_fn, float* __restrict__ out) {
-  extern __shared__ float wsm[];  // kRlPiece rows, row r at r*EP + (r/8)*4
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int t0 = (blockIdx.x * 8 + warp) * kRlTok;
-  float acc[kRlTok][EP];
-#pragma unroll
-  for (int a = 0; a < kRlTok; ++a)
-#pragma unroll
-    for (int e = 0; e < EP; ++e) acc[a][e] = 0.0f;
+struct RlShape {
+  static constexpr int COLS = 64 / EP;                   // columns of d per lane
+  static constexpr int TB = 32 / EP;                     // tokens per stage
+  static constexpr int SPAN = kRlWarps * 32 * COLS;      // columns per tile
+  static constexpr uint32_t STAGE = TB * SPAN * 2;       // bytes per stage
+  static constexpr int NS = int(kRlRingBytes / STAGE);   // stages
+};
 
-  for (int p0 = 0; p0 < d; p0 += kRlPiece) {
-    __syncthreads();
-    for (int i = threadIdx.x; i < kRlPiece * EP; i += blockDim.x) {
-      const int r = i / EP, e = i % EP;
-      const int dr = p0 + r;
-      wsm[r * EP + (r >> 3) * 4 + e] = (dr < d && e < E) ? __ldg(W + size_t(dr) * E + e) : 0.0f;
-    }
-    __syncthreads();
-    for (int r0 = 0; r0 < kRlPiece; r0 += 256) {
-      const int dcol = p0 + r0 + lane * 8;
-      if (dcol >= d) break;  // d % 8 == 0: a lane's 8 values are all in or all out
-      uint4 xv[kRlTok];
+// one butterfly step over N values: lanes with bit o set keep the upper half
+template <int N>
+__device__ __forceinline__ void transpose_reduce_step(float (&v)[32], int lane, int o) {
+  const bool up = (lane & o) != 0;
 #pragma unroll
-      for (int a = 0; a < kRlTok; ++a) {
-        const int t = t0 + a;
-        xv[a] = (t < T) ? __ldg(reinterpret_cast<const uint4*>(x + size_t(t) * d + dcol))
-                        : make_uint4(0, 0, 0, 0);
-      }
-      const float* wr = wsm + (r0 + lane * 8) * EP + ((r0 + lane * 8) >> 3) * 4;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        float w[EP];
-#pragma unroll
-        for (int e = 0; e < EP; e += 4) {
-          const float4 q = *reinterpret_cast<const float4*>(wr + i * EP + e);
-          w[e] = q.x; w[e + 1] = q.y; w[e + 2] = q.z; w[e + 3] = q.w;
-        }
-#pragma unroll
-        for (int a = 0; a < kRlTok; ++a) {
-          const uint32_t word = (&xv[a].x)[i >> 1];
-          const float xf = (i & 1) ? bf16hi(word) : bf16lo(word);
-#pragma unroll
-          for (int e = 0; e < EP; ++e) acc[a][e] = fmaf(xf, w[e], acc[a][e]);
-        }
+  for (int i = 0; i < N / 2; ++i) {
+    const float send = up ? v[i] : v[i + N / 2];
+    const float keep = up ? v[i + N / 2] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+  }
+}
+
+__device__ __forceinline__ bool rl_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                        int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*abort) return false;
+      if (global_ns() - t0 > kRlWaitNs) {
+        *abort = 1;
+        if (status) report_status(status, MOE_E_DEVICE_TIMEOUT);
+        return false;
       }
     }
   }
-#pragma unroll
-  for (int a = 0; a < kRlTok; ++a)
-#pragma unroll
-    for (int e = 0; e < EP; ++e) {
-      float v = acc[a][e];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      acc[a][e] = v;
+}
+
+template <int EP>
+__global__ void __launch_bounds__(kRlWarps * 32, 1) router_logits_small_kernel(
+    const __nv_bfloat16* __restrict__ x, const float* __restrict__ W, const float* __restrict__ lbias,
+    int T, int d, int E, int score_fn, int tpb, int* status, float* __restrict__ out) {
+  using S = RlShape<EP>;
+  constexpr int COLS = S::COLS, TB = S::TB, SPAN = S::SPAN, NS = S::NS;
+  extern __shared__ __align__(128) uint8_t smem_rl[];
+  uint8_t* ring = smem_rl;                                             // [NS][TB][SPAN] bf16
+  float* part = reinterpret_cast<float*>(smem_rl + size_t(NS) * S::STAGE);  // [warps][tpb][EP]
+  __shared__ uint64_t full[NS], empty[NS];
+  __shared__ int abort_flag;
+  volatile int* abort = &abort_flag;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t0 = blockIdx.x * tpb;
+  const int n_tok = min(T - t0, tpb);
+  const int n_b = (n_tok + TB - 1) / TB;   // stages per column tile
+  const int n_j = n_b * ((d + SPAN - 1) / SPAN);
+  float* mine = part + size_t(warp) * tpb * EP;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kRlWarps);
     }
-  if (lane < kRlTok) {
-    const int t = t0 + lane;
-    if (t < T) {
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // stage j: column tile j / n_b, tokens (j % n_b) * TB .. + TB (thread 0 only)
+  auto issue = [&](int j) {
+    const int q = j % NS, ct = j / n_b, b = j - ct * n_b;
+    const int rows = min(TB, n_tok - b * TB);
+    const uint32_t bytes = uint32_t(min(SPAN, d - ct * SPAN)) * 2;
+    mbar_arrive_expect_tx(&full[q], bytes * rows);
+    for (int a = 0; a < rows; ++a)
+      bulk_load_1d(ring + size_t(q) * S::STAGE + size_t(a) * SPAN * 2,
+                   x + size_t(t0 + b * TB + a) * d + size_t(ct) * SPAN, bytes, &full[q]);
+  };
+  int issued = 0;
+  if (threadIdx.x == 0)
+    for (; issued < min(NS, n_j); ++issued) issue(issued);
+
+  float2 w[COLS][EP / 2];  // expert pairs (e, e + 1), for packed fp32 FMAs
+  int ct_w = -1;
+  for (int j = 0; j < n_j; ++j) {
+    const int q = j % NS, ct = j / n_b, b = j - ct * n_b;
+    const uint32_t ph = uint32_t(j / NS) & 1u;
+    // this warp's first column in the tile; d % 64 == 0, so each 64-column
+    // group lies wholly inside or wholly past d.  Lane L takes columns
+    // g + 2L and g + 2L + 1 of each group g = cw + 64 i, i < COLS / 2.
+    const int cw = warp * 32 * COLS;
+    if (ct != ct_w) {
 #pragma unroll
-      for (int a = 0; a < kRlTok; ++a) {
-        if (a != lane) continue;
+      for (int i = 0; i < COLS / 2; ++i) {
+        const int c = ct * SPAN + cw + 64 * i + 2 * lane;  // even column
+        const bool in = c < d;
+        if (E == EP) {
+          // rows c, c + 1: 2 * EP consecutive floats
+          const float4* src = reinterpret_cast<const float4*>(W + size_t(c) * EP);
 #pragma unroll
-        for (int e = 0; e < EP; ++e) {
-          if (e >= E) break;
-          float l = acc[a][e];
-          if (lbias) l += __ldg(lbias + e);
-          if (score_fn == MOE_SIGMOID) l = 1.0f / (1.0f + expf(-l));
-          out[size_t(t) * E + e] = l;
+          for (int v4 = 0; v4 < EP / 2; ++v4) {
+            const float4 f = in ? __ldg(src + v4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int k = (4 * v4) / EP, e2 = ((4 * v4) % EP) / 2;
+            w[2 * i + k][e2] = make_float2(f.x, f.y);
+            w[2 * i + k][e2 + 1] = make_float2(f.z, f.w);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 2; ++k)
+#pragma unroll
+            for (int e2 = 0; e2 < EP / 2; ++e2) {
+              const int e = 2 * e2;
+              w[2 * i + k][e2] =
+                  make_float2((in && e < E) ? __ldg(W + size_t(c + k) * E + e) : 0.0f,
+                              (in && e + 1 < E) ? __ldg(W + size_t(c + k) * E + e + 1) : 0.0f);
+            }
         }
       }
+      ct_w = ct;
     }
+    const bool got = rl_wait(&full[q], ph, abort, status);
+    if (!__all_sync(0xffffffffu, got)) break;
+    // x words (bf16 pairs) of this lane's columns, token rows of the stage
+    const uint32_t* stg =
+        reinterpret_cast<const uint32_t*>(ring + size_t(q) * S::STAGE) + (cw >> 1) + lane;
+    uint32_t xw[TB][COLS / 2];
+#pragma unroll
+    for (int a = 0; a < TB; ++a) {
+      const bool row_in = b * TB + a < n_tok;
+#pragma unroll
+      for (int i = 0; i < COLS / 2; ++i) {
+        const bool ok = row_in && ct * SPAN + cw + 64 * i < d;
+        xw[a][i] = ok ? stg[a * (SPAN / 2) + 32 * i] : 0u;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[q]);
+    float v[32];
+#pragma unroll
+    for (int a = 0; a < TB; ++a)
+#pragma unroll
+      for (int e2 = 0; e2 < EP / 2; ++e2) {
+        float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int i = 0; i < COLS; ++i) {
+          const float xf = (i & 1) ? bf16hi(xw[a][i >> 1]) : bf16lo(xw[a][i >> 1]);
+          acc = __ffma2_rn(make_float2(xf, xf), w[i][e2], acc);  // two fmaf in one
+        }
+        v[a * EP + 2 * e2] = acc.x;
+        v[a * EP + 2 * e2 + 1] = acc.y;
+      }
+    transpose_reduce_step<32>(v, lane, 16);
+    transpose_reduce_step<16>(v, lane, 8);
+    transpose_reduce_step<8>(v, lane, 4);
+    transpose_reduce_step<4>(v, lane, 2);
+    transpose_reduce_step<2>(v, lane, 1);
+    {
+      const int a = lane / EP, e = lane % EP;
+      if (b * TB + a < n_tok) {
+        float* slot = mine + (b * TB + a) * EP + e;
+        *slot = ct == 0 ? v[0] : *slot + v[0];
+      }
+    }
+    // refill this stage once every warp has read it
+    if (warp == 0 && j + NS < n_j) {
+      bool freed = true;
+      if (lane == 0) {
+        freed = rl_wait(&empty[q], ph, abort, status);
+        if (freed) issue(issued++);
+      }
+      if (!__shfl_sync(0xffffffffu, freed ? 1 : 0, 0)) break;
+    }
+  }
+  if (threadIdx.x == 0 && *abort) {
+    // copies still in flight land before the block exits
+    for (int k = max(0, issued - NS); k < issued; ++k)
+      mbar_wait_bounded(&full[k % NS], uint32_t(k / NS) & 1u, kRlDrainNs);
+  }
+  __syncthreads();
+  if (*abort) return;
+  for (int i = threadIdx.x; i < n_tok * E; i += blockDim.x) {
+    const int a = i / E, e = i - a * E;
+    float l = 0.0f;
+#pragma unroll
+    for (int w2 = 0; w2 < kRlWarps; ++w2) l += part[(size_t(w2) * tpb + a) * EP + e];
+    if (lbias) l += __ldg(lbias + e);
+    if (score_fn == MOE_SIGMOID) l = 1.0f / (1.0f + expf(-l));
+    out[size_t(t0 + a) * E + e] = l;
   }
 }
 
@@ -317,25 +446,36 @@ __global__ void __launch_bounds__(256) router_logits_tiled_kernel(
 // Host launchers
 // ---------------------------------------------------------------------------
 int launch_router_logits(const moe_cfg& c, const void* x, const float* W, const float* lbias,
-                         float* out, cudaStream_t st) {
+                         float* out, int* status, cudaStream_t st) {
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   if (c.E <= 16) {
-    const int blocks = (c.T + 8 * kRlTok - 1) / (8 * kRlTok);
-    if (c.E <= 8) {
-      const size_t sm = size_t(kRlPiece) * 8 * 4 + (kRlPiece / 8) * 16;
-      router_logits_small_kernel<8><<<blocks, 256, sm, st>>>(xb, W, lbias, c.T, c.d, c.E,
-                                                             c.score_fn, out);
-    } else {
-      const size_t sm = size_t(kRlPiece) * 16 * 4 + (kRlPiece / 8) * 16;
-      static bool attr = false;
-      if (!attr) {
-        cudaFuncSetAttribute(router_logits_small_kernel<16>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
-        attr = true;
-      }
-      router_logits_small_kernel<16><<<blocks, 256, sm, st>>>(xb, W, lbias, c.T, c.d, c.E,
-                                                              c.score_fn, out);
-    }
+    // tokens per block: the tokens spread over the SMs, whole stages, at most kRlMaxTok
+    const int sms = device_sm_count();
+    if (sms <= 0) return MOE_E_CUDA;
+    const int ep = c.E <= 8 ? 8 : 16;
+    const int tb = 32 / ep;
+    int tpb = (c.T + sms - 1) / sms;
+    tpb = (tpb + tb - 1) / tb * tb;
+    if (tpb > kRlMaxTok) tpb = kRlMaxTok;
+    const int blocks = (c.T + tpb - 1) / tpb;
+    const size_t sm = kRlRingBytes + size_t(kRlWarps) * tpb * ep * 4;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+      const int mx = int(kRlRingBytes + size_t(kRlWarps) * kRlMaxTok * 16 * 4);
+      attr_err = cudaFuncSetAttribute(router_logits_small_kernel<8>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+      if (attr_err == cudaSuccess)
+        attr_err = cudaFuncSetAttribute(router_logits_small_kernel<16>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    });
+    if (attr_err != cudaSuccess) return MOE_E_CUDA;
+    if (ep == 8)
+      router_logits_small_kernel<8><<<blocks, kRlWarps * 32, sm, st>>>(
+          xb, W, lbias, c.T, c.d, c.E, c.score_fn, tpb, status, out);
+    else
+      router_logits_small_kernel<16><<<blocks, kRlWarps * 32, sm, st>>>(
+          xb, W, lbias, c.T, c.d, c.E, c.score_fn, tpb, status, out);
   } else {
     dim3 grid((c.T + 63) / 64, (c.E + 63) / 64);
     router_logits_tiled_kernel<<<grid, 256, 0, st>>>(xb, W, lbias, c.T, c.d, c.E, c.score_fn, out);

@@ -278,6 +278,36 @@ def test_router_logits_parity(m, name, tc):
         assert np.median(np.abs(got - l_ref)) < 1e-5
 
 
+@pytest.mark.parametrize("E,d,T,sig", [
+    (1, 64, 1, False), (3, 192, 7, True), (4, 1088, 29, False), (5, 8256, 300, True),
+    (8, 4160, 1000, False), (8, 8256, 9001, True), (13, 64, 61, False), (16, 2112, 4099, True),
+    (16, 8256, 33, False)])
+def test_router_logits_simt_shapes(m, E, d, T, sig):
+    """The fp32 SIMT router (E <= 16) at the shapes its tiling has edges: d
+    smaller than one column tile (idle warps), d over one or two tiles with a
+    partial last tile, token counts that leave a ragged last batch and block,
+    one token, one expert; with logit bias, and sigmoid scores."""
+    g = torch.Generator().manual_seed(E * 100003 + d * 7 + T)
+    cfg = C["tiny"].with_(T=T, d=d, E=E, k=1, n_ep=1, score_fn="sigmoid" if sig else "softmax",
+                          norm_topk=int(sig))
+    x = torch.randn(T, d, generator=g).bfloat16()
+    W_r = (torch.randn(d, E, generator=g) / math.sqrt(d)).float()
+    lb = (torch.randn(E, generator=g) * 0.5).float()
+    c = m.MoeCfg.from_layer(cfg)
+    out = torch.full((T, E), float("nan"), dtype=torch.float32, device="cuda")
+    m.moe_router_logits(c, x.cuda(), W_r.cuda(), None, lb.cuda(), out)
+    torch.cuda.synchronize()
+    xf, Wf = x.float().numpy(), W_r.numpy()
+    l_ref = oracle.router_logits(xf, Wf, lb.numpy())
+    bound = _logit_bound(xf, Wf) + 2.0 ** -24 * np.abs(l_ref) + 1e-30
+    got = npf(out)
+    assert np.isfinite(got).all()
+    if sig:
+        assert (np.abs(got - oracle.sigmoid(l_ref)) <= 0.25 * bound + 4e-7).all()
+    else:
+        assert (np.abs(got - l_ref) <= bound).all()
+
+
 def test_router_split_is_exact(m):
     """hi + mid + lo reproduces every fp32 router weight exactly."""
     cfg = SMALL["ds_small"]
