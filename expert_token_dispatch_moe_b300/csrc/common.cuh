@@ -18,7 +18,7 @@ namespace moe {
 //                  permute histogram (uint32 at 8, back to 0 after each call)
 //   src_cnt        int32 [n_ep][E]   assignments per (source rank, expert)
 //   chunk_hist     int32 [n_chunks][E] per-chunk histogram, then chunk bases
-//   ep_sbase       int32 [n_ep][E]   send-slot base for (s, e)
+//   ep_sbase       int32 [n_ep][E]   (unused: the layout kernel keeps these bases in shared memory)
 //   send_pos       int32 [A]         send slot of each assignment (-1 dropped)
 // ---------------------------------------------------------------------------
 constexpr int kPermChunk = 2048;   // assignments per histogram/rank CTA

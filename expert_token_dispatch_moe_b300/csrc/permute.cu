@@ -17,6 +17,8 @@
 //             its k copies.
 // Capacity mode keeps rank < cap at row e*cap + rank and zero-fills the rest
 // of each segment (one warp per row, over the whole grouped buffer).
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -193,6 +195,137 @@ __global__ void __launch_bounds__(kPermThreads) perm_rank_kernel(
 }
 
 // ---------------------------------------------------------------------------
+// 1+2 in one CTA, for small batches (A <= kPermSmallMaxA, E <= kPermSmallMaxE):
+// no chunk tables, no cross-CTA hand-off, one launch.  Pass 1 counts experts
+// (and (source rank, expert) pairs) and scans them into offsets; pass 2 walks
+// the assignments in rounds of 1024 in index order: warp match/popc ranks
+// within a warp, then per expert an exclusive scan over the 32 warps (one
+// warp per expert, a lane per warp) on top of the expert's count from earlier
+// rounds.  Per-warp counts are tagged with the round, so the table never needs
+// clearing.
+// ---------------------------------------------------------------------------
+constexpr int kPermSmallThreads = 1024;
+constexpr int kPermSmallMaxA = 4096;
+constexpr int kPermSmallMaxE = 256;
+
+__global__ void __launch_bounds__(kPermSmallThreads, 1) perm_index_small_kernel(
+    const int32_t* __restrict__ idx, int A, int E, int k, int T_loc, int n_ep, int capacity,
+    int32_t* __restrict__ src_cnt, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ inv, int32_t* __restrict__ order, int* status) {
+  extern __shared__ int32_t sm_small[];
+  const int ld = E + 1;                  // row pitch of the warp tables (odd: no bank conflicts)
+  int32_t* tab = sm_small;               // [32][ld]: (round << 16) | count of e in warp w
+  int32_t* pre = sm_small + 32 * ld;     // [32][ld]: rank base of e for warp w this round
+  int32_t* base = sm_small + 64 * ld;    // [E]: first row of e (dropless)
+  int32_t* seen = base + E;              // [E]: assignments of e in earlier rounds
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int i = tid; i < 32 * ld; i += blockDim.x) tab[i] = -1;  // tag -1: no round
+  for (int e = tid; e < E; e += blockDim.x) { base[e] = 0; seen[e] = 0; }
+  for (int i = tid; i < n_ep * E; i += blockDim.x) src_cnt[i] = 0;
+  // every expert id this thread will touch, loaded at once (assignment
+  // r * 1024 + tid in round r); -1 past the end or for an invalid id
+  constexpr int ROUNDS = kPermSmallMaxA / kPermSmallThreads;
+  int ev[ROUNDS];
+#pragma unroll
+  for (int r = 0; r < ROUNDS; ++r) {
+    const int a = r * kPermSmallThreads + tid;
+    ev[r] = a < A ? __ldg(idx + a) : -1;
+  }
+#pragma unroll
+  for (int r = 0; r < ROUNDS; ++r) {
+    const int a = r * kPermSmallThreads + tid;
+    if (a < A && (ev[r] < 0 || ev[r] >= E)) {
+      report_status(status, MOE_E_DEVICE_DATA);
+      ev[r] = -1;
+    }
+  }
+  __syncthreads();
+
+  // pass 1: expert totals and per-(source rank, expert) counts
+#pragma unroll
+  for (int r = 0; r < ROUNDS; ++r) {
+    if (r * kPermSmallThreads >= A) break;
+    const int a = r * kPermSmallThreads + tid;
+    const int e = ev[r];
+    const int key = e >= 0 ? ((a / k) / T_loc) * E + e : -1;
+    const uint32_t pe = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && (pe & lt) == 0) atomicAdd(&base[e], __popc(pe));
+    const uint32_t pk = __match_any_sync(0xffffffffu, key);
+    if (key >= 0 && (pk & lt) == 0) atomicAdd(src_cnt + key, __popc(pk));
+  }
+  __syncthreads();
+  // counts and offsets: warp 0 scans the totals (8 experts per lane at most)
+  if (warp == 0) {
+    constexpr int PER = kPermSmallMaxE / 32;
+    int v[PER], local = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane * PER + i;
+      v[i] = e < E ? base[e] : 0;
+      local += v[i];
+    }
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    int run = incl - local;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane * PER + i;
+      if (e < E) {
+        counts[e] = v[i];
+        offsets[e] = capacity ? e * capacity : run;
+        base[e] = run;
+      }
+      run += v[i];
+    }
+    if (lane == 31) offsets[E] = capacity ? E * capacity : run;
+  }
+  __syncthreads();
+
+  // pass 2: stable ranks, 1024 assignments per round in index order
+#pragma unroll
+  for (int r = 0; r < ROUNDS; ++r) {
+    if (r * kPermSmallThreads >= A) break;
+    const int a = r * kPermSmallThreads + tid;
+    const int e = ev[r];
+    const uint32_t pe = __match_any_sync(0xffffffffu, e);
+    const int lrank = __popc(pe & lt);
+    if (e >= 0 && lrank == 0) tab[warp * ld + e] = (r << 16) | __popc(pe);
+    __syncthreads();
+    // warp w scans experts w, w + 32, ...: lane l holds warp l's count
+    for (int e2 = warp; e2 < E; e2 += 32) {
+      const int tv = tab[lane * ld + e2];
+      const int c = (tv >> 16) == r ? (tv & 0xffff) : 0;
+      int incl = c;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      const int before = seen[e2];
+      pre[lane * ld + e2] = before + incl - c;
+      __syncwarp();
+      if (lane == 31) seen[e2] = before + incl;
+    }
+    __syncthreads();
+    if (a < A) {
+      int row = -1;
+      if (e >= 0) {
+        const int rank = pre[warp * ld + e] + lrank;
+        if (capacity) row = rank < capacity ? e * capacity + rank : -1;
+        else row = base[e] + rank;
+      }
+      inv[a] = row;
+      if (row >= 0) order[row] = a;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // 3. row move: one warp per token, x[t] read once, written to its k rows.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) row_scatter_kernel(const uint4* __restrict__ x, int T,
@@ -256,10 +389,21 @@ __global__ void __launch_bounds__(256) perm_pad_kernel(const int32_t* __restrict
 //   send_off[s][q] = sum_{e<q*G} kept[e]
 //   recv_off[q][s] = rows q received from ranks < s
 //                  = sum over q's experts of before[e] (or min(before[e], cap)).
-__global__ void __launch_bounds__(kPermThreads) ep_tables_kernel(
-    const int32_t* __restrict__ src_cnt, int n_ep, int E, int k, int T_loc, int capacity,
-    int32_t* __restrict__ sbase, int32_t* __restrict__ C, int32_t* __restrict__ send_off,
-    int32_t* __restrict__ recv_off) {
+//
+// CTA (s, j) computes the tables of source rank s (every CTA of the rank
+// recomputes them; CTA (s, 0) writes them out) and then places the rank's
+// assignments j*kEpPerCta .. (j+1)*kEpPerCta - 1: slot(a) = sbase[s][e] +
+// rank(a) for each kept assignment a (send_pos[a], -1 when dropped;
+// send_idx[slot] = a), and marks the rank's slots past its kept rows empty
+// (send_idx = -1).
+constexpr int kEpPerCta = 1024;  // assignments placed per CTA
+
+__global__ void __launch_bounds__(kPermThreads) ep_layout_kernel(
+    const int32_t* __restrict__ src_cnt, const int32_t* __restrict__ idx,
+    const int32_t* __restrict__ inv, const int32_t* __restrict__ offsets, int n_ep, int E, int k,
+    int T_loc, int capacity, int32_t* __restrict__ C, int32_t* __restrict__ send_off,
+    int32_t* __restrict__ recv_off, int32_t* __restrict__ send_idx,
+    int32_t* __restrict__ send_pos) {
   extern __shared__ int32_t sm[];
   int32_t* kept = sm;              // [E + 1] -> exclusive prefix
   int32_t* recv = sm + E + 1;      // [E + 1] -> exclusive prefix
@@ -287,41 +431,31 @@ __global__ void __launch_bounds__(kPermThreads) ep_tables_kernel(
     recv[E] = recv_all;
   }
   __syncthreads();
-  const int base = s * T_loc * k;
-  for (int e = threadIdx.x; e < E; e += blockDim.x)
-    sbase[size_t(s) * E + e] = base + kept[e] - bef[e];
   const int G = E / n_ep;
-  for (int q = threadIdx.x; q < n_ep; q += blockDim.x) {
-    C[size_t(s) * n_ep + q] = kept[(q + 1) * G] - kept[q * G];
-    send_off[size_t(s) * n_ep + q] = kept[q * G];
-    recv_off[size_t(q) * n_ep + s] = recv[(q + 1) * G] - recv[q * G];
+  if (blockIdx.y == 0) {
+    for (int q = threadIdx.x; q < n_ep; q += blockDim.x) {
+      C[size_t(s) * n_ep + q] = kept[(q + 1) * G] - kept[q * G];
+      send_off[size_t(s) * n_ep + q] = kept[q * G];
+      recv_off[size_t(q) * n_ep + s] = recv[(q + 1) * G] - recv[q * G];
+    }
   }
-}
-
-// Per assignment a: its send slot (send_pos[a], -1 when dropped) and
-// send_idx[slot] = a.  Thread p also marks slot p empty (send_idx = -1) when
-// it lies past its rank's kept rows (capacity drops, or invalid expert ids).
-__global__ void __launch_bounds__(256) ep_scatter_kernel(
-    const int32_t* __restrict__ idx, const int32_t* __restrict__ inv,
-    const int32_t* __restrict__ offsets, const int32_t* __restrict__ sbase,
-    const int32_t* __restrict__ C, const int32_t* __restrict__ send_off, int A, int E, int k,
-    int T_loc, int n_ep, int32_t* __restrict__ send_idx, int32_t* __restrict__ send_pos) {
-  const int a = blockIdx.x * blockDim.x + threadIdx.x;
-  if (a >= A) return;
-  const int e = __ldg(idx + a);
-  const int row = __ldg(inv + a);
   const int rpr = T_loc * k;
-  const int s = a / rpr;
-  int p = -1;
-  if (row >= 0 && e >= 0 && e < E) {
-    const int rank = row - __ldg(offsets + e);
-    p = __ldg(sbase + size_t(s) * E + e) + rank;
-    send_idx[p] = a;
+  const int base = s * rpr;
+  for (int j = blockIdx.y; j * kEpPerCta < rpr; j += gridDim.y) {
+    const int i_end = min(rpr, (j + 1) * kEpPerCta);
+    for (int i = j * kEpPerCta + threadIdx.x; i < i_end; i += blockDim.x) {
+      const int a = base + i;
+      const int e = __ldg(idx + a);
+      const int row = __ldg(inv + a);
+      int p = -1;
+      if (row >= 0 && e >= 0 && e < E) {
+        p = base + kept[e] + (row - __ldg(offsets + e)) - bef[e];
+        send_idx[p] = a;
+      }
+      send_pos[a] = p;
+      if (i >= kept_all) send_idx[a] = -1;  // slot a is past the rank's kept rows
+    }
   }
-  send_pos[a] = p;
-  const size_t last = size_t(s) * n_ep + n_ep - 1;
-  const int used = __ldg(send_off + last) + __ldg(C + last);
-  if (a - s * rpr >= used) send_idx[a] = -1;
 }
 
 // Zero the send-buffer rows past each rank's kept rows (slot p of rank
@@ -371,13 +505,31 @@ int launch_permute(const moe_cfg& c, const void* x, const int32_t* idx, int32_t*
   unsigned int* done = ws_ptr<unsigned int>(ws, L.done_ctas);
   int32_t* src_cnt = ws_ptr<int32_t>(ws, L.src_cnt);
   int32_t* chunk_hist = ws_ptr<int32_t>(ws, L.chunk_hist);
-  if (cudaMemsetAsync(src_cnt, 0, size_t(c.n_ep) * c.E * 4, st) != cudaSuccess) return MOE_E_CUDA;
-  perm_hist_kernel<<<L.n_chunks, kPermThreads, c.E * 4, st>>>(
-      idx, A, c.E, c.k, c.T / c.n_ep, c.capacity, chunk_hist, src_cnt, counts, offsets, status,
-      done);
-  perm_rank_kernel<<<L.n_chunks, kPermThreads, 8 * c.E * 4, st>>>(idx, A, c.E, c.capacity,
-                                                                  chunk_hist, offsets, inv, order);
-  note_launches(2);
+  if (A <= kPermSmallMaxA && c.E <= kPermSmallMaxE) {
+    // one CTA does the histogram, the scans and the ranks
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+      attr_err = cudaFuncSetAttribute(perm_index_small_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      int((64 * (kPermSmallMaxE + 1) + 2 * kPermSmallMaxE) * 4));
+    });
+    if (attr_err != cudaSuccess) return MOE_E_CUDA;
+    const size_t smem = size_t(64 * (c.E + 1) + 2 * c.E) * 4;
+    perm_index_small_kernel<<<1, kPermSmallThreads, smem, st>>>(
+        idx, A, c.E, c.k, c.T / c.n_ep, c.n_ep, c.capacity, src_cnt, counts, offsets, inv, order,
+        status);
+    note_launches(1);
+  } else {
+    if (cudaMemsetAsync(src_cnt, 0, size_t(c.n_ep) * c.E * 4, st) != cudaSuccess)
+      return MOE_E_CUDA;
+    perm_hist_kernel<<<L.n_chunks, kPermThreads, c.E * 4, st>>>(
+        idx, A, c.E, c.k, c.T / c.n_ep, c.capacity, chunk_hist, src_cnt, counts, offsets, status,
+        done);
+    perm_rank_kernel<<<L.n_chunks, kPermThreads, 8 * c.E * 4, st>>>(
+        idx, A, c.E, c.capacity, chunk_hist, offsets, inv, order);
+    note_launches(2);
+  }
   if (c.capacity) {
     const int R = c.E * c.capacity;
     perm_pad_kernel<<<row_grid(R), 256, 0, st>>>(counts, c.capacity, R, c.d / 8, order,
@@ -397,14 +549,14 @@ int launch_ep_layout(const moe_cfg& c, const int32_t* idx, const int32_t* offset
   const int A = c.T * c.k;
   const int T_loc = c.T / c.n_ep;
   int32_t* src_cnt = ws_ptr<int32_t>(ws, L.src_cnt);
-  int32_t* sbase = ws_ptr<int32_t>(ws, L.ep_sbase);
   int32_t* send_pos = ws_ptr<int32_t>(ws, L.send_pos);
   const size_t smem = size_t(3 * c.E + 2) * 4;
-  ep_tables_kernel<<<c.n_ep, kPermThreads, smem, st>>>(src_cnt, c.n_ep, c.E, c.k, T_loc,
-                                                       c.capacity, sbase, C, send_off, recv_off);
-  ep_scatter_kernel<<<(A + 255) / 256, 256, 0, st>>>(idx, inv, offsets, sbase, C, send_off, A,
-                                                     c.E, c.k, T_loc, c.n_ep, send_idx, send_pos);
-  note_launches(2);
+  const int per_rank = (T_loc * c.k + kEpPerCta - 1) / kEpPerCta;
+  const dim3 grid(c.n_ep, per_rank < 65535 ? per_rank : 65535);
+  ep_layout_kernel<<<grid, kPermThreads, smem, st>>>(src_cnt, idx, inv, offsets, c.n_ep, c.E,
+                                                       c.k, T_loc, c.capacity, C, send_off,
+                                                       recv_off, send_idx, send_pos);
+  note_launches(1);
   if (cudaGetLastError() != cudaSuccess) return MOE_E_CUDA;
   if (x && send_buf) {
     if (c.capacity) {
