@@ -34,7 +34,7 @@ EXPORTS = ("moe_validate_cfg", "moe_grouped_rows", "moe_workspace_bytes", "moe_w
            "moe_grouped_ffn", "moe_grouped_ffn_gather", "moe_grouped_ffn_train", "moe_combine", "moe_bias_update", "moe_eplb_plan",
            "moe_eplb_dispatch", "moe_pack_backward", "moe_combine_backward",
            "moe_backward_workspace_bytes", "moe_grouped_ffn_backward", "moe_permute_backward",
-           "moe_get_device_status", "moe_strerror",
+           "moe_selftest_wait_timeout", "moe_get_device_status", "moe_strerror",
            "moe_last_launch_count")
 
 
@@ -103,6 +103,7 @@ _sig = {
     "moe_grouped_ffn_train": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                              _P]),
     "moe_permute_backward": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
+    "moe_selftest_wait_timeout": (ctypes.c_int, [_P, ctypes.c_uint64, _P]),
     "moe_get_device_status": (ctypes.c_int, [_P, _P]),
     "moe_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_last_launch_count": (ctypes.c_int, []),
@@ -296,6 +297,11 @@ def moe_grouped_ffn_train(cfg, x_sorted, x, counts, offsets, W13, W2, h, y_sorte
 def moe_permute_backward(cfg, dx_sorted, inv, dx, stream=None):
     _check(_lib.moe_permute_backward(ctypes.byref(cfg), _ptr(dx_sorted), _ptr(inv), _ptr(dx),
                                      _stream(stream)), "moe_permute_backward")
+
+
+def moe_selftest_wait_timeout(ws, limit_ns, stream=None):
+    _check(_lib.moe_selftest_wait_timeout(_ptr(ws), int(limit_ns), _stream(stream)),
+           "moe_selftest_wait_timeout")
 
 
 def moe_get_device_status(ws, stream=None) -> int:

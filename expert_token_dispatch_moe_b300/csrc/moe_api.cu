@@ -391,6 +391,31 @@ MOE_API int moe_permute_backward(const moe_cfg* c, const moe_bf16* dx_sorted, co
   return launch_combine(*c, dx_sorted, inv, nullptr, dx, static_cast<cudaStream_t>(stream));
 }
 
+// One CTA waits on an mbarrier whose phase never completes; the bounded wait
+// gives up after limit_ns and the kernel reports the time-out and returns.
+__global__ void wait_timeout_selftest_kernel(int* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait_bounded(&bar, 0, limit_ns))
+    report_status(status, MOE_E_DEVICE_TIMEOUT);
+}
+
+MOE_API int moe_selftest_wait_timeout(void* ws, uint64_t limit_ns, void* stream) {
+  reset_launches();
+  if (!ws) return MOE_E_WORKSPACE;
+  if (!aligned16(ws)) return MOE_E_ALIGN;
+  if (limit_ns < 1000ull || limit_ns > 1000000000ull) return MOE_E_SHAPE;
+  MOE_TRY(device_ok());
+  wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<int*>(ws), limit_ns);
+  note_launches(1);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_E_CUDA;
+}
+
 MOE_API int moe_get_device_status(void* ws, void* stream) {
   reset_launches();
   if (!ws) return MOE_E_WORKSPACE;

@@ -81,8 +81,9 @@ class MoELayer:
         self.launches_per_backward = None
         self.W13t = None        # backward buffers, allocated on the first backward
 
-    def forward(self, x, scores=None):
-        """Run the layer on device tokens x (bf16 [T, d]); returns self.y.
+    def forward(self, x, scores=None, y=None):
+        """Run the layer on device tokens x (bf16 [T, d]); returns self.y, or
+        `y` (bf16 [T, d] on the device) when given.
 
         With `scores` (fp32 [T, E]) the router step is skipped and the given
         scores are routed (used to check routing on exact inputs)."""
@@ -117,10 +118,11 @@ class MoELayer:
             moe_grouped_ffn(c, self.x_sorted, x if c.has_shared else None, self.counts,
                             self.offsets, self.W13, self.W2, self.h, self.y_sorted, self.ws)
         n += moe_last_launch_count()
-        moe_combine(c, self.y_sorted, self.inv, self.topk_gate, self.y)
+        out = self.y if y is None else y
+        moe_combine(c, self.y_sorted, self.inv, self.topk_gate, out)
         n += moe_last_launch_count()
         self.launches_per_forward = n
-        return self.y
+        return out
 
     __call__ = forward
 
@@ -164,6 +166,53 @@ class MoELayer:
         n, f2, d = self.dW13.shape
         blk = self.dW13.view(n, f2 // 256, 2, 128, d)
         return blk[:, :, 0].reshape(n, f2 // 2, d), blk[:, :, 1].reshape(n, f2 // 2, d)
+
+    def forward_host_stream(self, x_hosts, y_hosts):
+        """Runs the layer on a sequence of host batches (pinned bf16 [T, d] each)
+        and writes each result into the matching pinned host buffer.  Batch i's
+        host-to-device copy and batch i-1's device-to-host copy run on their own
+        streams while batch i-1 (resp. i) computes, with two device buffers on
+        each side; the compute stream is the caller's current stream.  Returns
+        when all copies have been enqueued (synchronise the current stream to
+        wait for the last result)."""
+        comp = torch.cuda.current_stream(self.device)
+        s_in, s_out = self._copy_streams()
+        T, d = self.cfg.T, self.cfg.d
+        if getattr(self, "_xbuf", None) is None:
+            self._xbuf = [torch.empty(T, d, dtype=torch.bfloat16, device=self.device)
+                          for _ in range(2)]
+            self._ybuf = [torch.empty(T, d, dtype=torch.bfloat16, device=self.device)
+                          for _ in range(2)]
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+        start = ev()
+        start.record(comp)
+        s_in.wait_event(start)
+        for i, (xh, yh) in enumerate(zip(x_hosts, y_hosts)):
+            b = i & 1
+            if i >= 2:
+                s_in.wait_event(comp_done[b])     # batch i-2 no longer reads xbuf[b]
+            with torch.cuda.stream(s_in):
+                self._xbuf[b].copy_(xh, non_blocking=True)
+            in_done[b].record(s_in)
+            comp.wait_event(in_done[b])
+            if i >= 2:
+                comp.wait_event(out_done[b])      # batch i-2's result has left ybuf[b]
+            self.forward(self._xbuf[b], y=self._ybuf[b])
+            comp_done[b].record(comp)
+            s_out.wait_event(comp_done[b])
+            with torch.cuda.stream(s_out):
+                yh.copy_(self._ybuf[b], non_blocking=True)
+            out_done[b].record(s_out)
+        n = len(x_hosts)
+        for b in range(min(n, 2)):
+            comp.wait_event(out_done[b])
+        return y_hosts
+
+    def _copy_streams(self):
+        if getattr(self, "_streams", None) is None:
+            self._streams = (torch.cuda.Stream(self.device), torch.cuda.Stream(self.device))
+        return self._streams
 
     def forward_host(self, x_host, y_host, x_dev=None):
         """End-to-end call with host buffers: copies pinned host x to the

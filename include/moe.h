@@ -411,6 +411,17 @@ int moe_eplb_dispatch(const moe_cfg* cfg, const int32_t* topk_idx, const int32_t
                       const int32_t* copy_offset, const int32_t* copy_rank, int32_t* dest_rank,
                       int32_t* count_mat, void* stream);
 
+/* Self-test of the device-side time-out path that every kernel with a wait
+ * uses.  Launches one small CTA that waits, through the same bounded
+ * mbarrier wait, on a barrier that nothing ever completes; after limit_ns it
+ * gives up, records MOE_E_DEVICE_TIMEOUT in the workspace status word and
+ * returns, leaving the context usable.  No fault, trap or hang is involved.
+ *   ws         workspace of at least moe_workspace_bytes(cfg) for any cfg
+ *              (only the status word at offset 0 is touched), 16-byte aligned
+ *   limit_ns   how long the wait lasts, 1000 .. 1000000000 (else MOE_E_SHAPE)
+ * Asynchronous on `stream`; read the result with moe_get_device_status. */
+int moe_selftest_wait_timeout(void* ws, uint64_t limit_ns, void* stream);
+
 /* Synchronises `stream`, then returns and clears the workspace status word:
  * MOE_OK, MOE_E_DEVICE_DATA or MOE_E_DEVICE_TIMEOUT (or MOE_E_CUDA). */
 int moe_get_device_status(void* ws, void* stream);

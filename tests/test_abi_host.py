@@ -94,5 +94,11 @@ def test_host_argument_errors(m):
         assert lib.moe_route(cfg, P, None, P, P, None) == -6
         assert lib.moe_combine(cfg, P, P, P, P, None) == -6
     assert lib.moe_get_device_status(None, None) == -4
+    assert lib.moe_selftest_wait_timeout(None, 10 ** 6, None) == -4
+    assert lib.moe_selftest_wait_timeout(P + 4, 10 ** 6, None) == -3
+    assert lib.moe_selftest_wait_timeout(P, 999, None) == -2
+    assert lib.moe_selftest_wait_timeout(P, 10 ** 9 + 1, None) == -2
+    if not torch.cuda.is_available():
+        assert lib.moe_selftest_wait_timeout(P, 10 ** 6, None) == -6
     for code in range(-8, 1):
         assert lib.moe_strerror(code)

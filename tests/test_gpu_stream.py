@@ -1,0 +1,30 @@
+"""The streaming host call: several host batches through
+MoELayer.forward_host_stream (copies on their own streams, overlapping
+compute, two device buffers per side) give, batch for batch, exactly the
+outputs of the plain device forward."""
+import pytest
+import torch
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name,n", [("tiny", 5), ("mixtral", 3)])
+def test_forward_host_stream_matches_device_forward(name, n):
+    import expert_token_dispatch_moe_b300 as m
+    cfg = synth.CONFIGS[name]
+    if name == "mixtral":
+        cfg = cfg.with_(T=512)   # the full expert shapes, fewer tokens
+    W1, W3, W2 = synth.make_expert_weights(cfg, device="cuda")
+    W_r, lb = synth.make_router(cfg, device="cuda")
+    layer = m.MoELayer(cfg, W1, W3, W2, W_r=W_r, logit_bias=lb)
+    xs = [synth.make_x(cfg, seed=100 + i).pin_memory() for i in range(n)]
+    ys = [torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory() for _ in range(n)]
+    layer.forward_host_stream(xs, ys)
+    torch.cuda.synchronize()
+    for i in range(n):
+        ref = layer.forward(xs[i].cuda()).cpu()
+        torch.cuda.synchronize()
+        assert torch.equal(ys[i].view(torch.int16), ref.view(torch.int16)), i
+    assert m.moe_get_device_status(layer.ws) == 0
