@@ -19,47 +19,97 @@
 namespace moe {
 
 // ---------------------------------------------------------------------------
-// step 7 backward: one warp per token
+// step 7 backward: one warp per token.  KT > 0 (k known at compile time): per
+// pass a lane loads U vectors of dy once and the matching vectors of all k
+// expert rows together, so about 8-16 loads are in flight per lane; KT == 0
+// walks the k rows one after another.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 scale_dot_bf16x8(const uint4& dv, const uint4& ov, float g,
+                                                  float& dot) {
+  const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w}, ow[4] = {ov.x, ov.y, ov.z, ov.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float d0 = bf16lo(dw[i]), d1 = bf16hi(dw[i]);
+    dot = fmaf(d0, bf16lo(ow[i]), dot);
+    dot = fmaf(d1, bf16hi(ow[i]), dot);
+    out[i] = pack_bf16x2(g * d0, g * d1);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+template <int KT>
 __global__ void __launch_bounds__(256) combine_backward_kernel(
     const uint4* __restrict__ dy, const uint4* __restrict__ y_sorted,
-    const int32_t* __restrict__ inv, const float* __restrict__ gate, int T, int k, int vec, int R,
-    int has_shared, uint4* __restrict__ d_o, float* __restrict__ dgate) {
+    const int32_t* __restrict__ inv, const float* __restrict__ gate, int T, int k_rt, int vec,
+    int R, int has_shared, uint4* __restrict__ d_o, float* __restrict__ dgate) {
+  const int k = KT > 0 ? KT : k_rt;
   const int lane = threadIdx.x & 31;
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
   const uint4* dyr = dy + size_t(t) * vec;
-  for (int j = 0; j < k; ++j) {
-    const int a = t * k + j;
-    const int row = __ldg(inv + a);
-    if (row < 0) {
-      if (lane == 0) dgate[a] = 0.0f;
-      continue;
-    }
-    const float g = __ldg(gate + a);
-    const uint4* orow = y_sorted + size_t(row) * vec;
-    uint4* drow = d_o + size_t(row) * vec;
-    float dot = 0.0f;
-    for (int v = lane; v < vec; v += 32) {
-      const uint4 dv = __ldg(dyr + v), ov = __ldg(orow + v);
-      const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w}, ow[4] = {ov.x, ov.y, ov.z, ov.w};
-      uint32_t out[4];
+  uint4* shared_row = d_o + size_t(R + t) * vec;
+  if constexpr (KT > 0) {
+    const int my_row = (lane < KT) ? __ldg(inv + size_t(t) * KT + lane) : -1;
+    const float my_g = (lane < KT) ? __ldg(gate + size_t(t) * KT + lane) : 0.0f;
+    int rows[KT];
+    float gs[KT], dot[KT];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float d0 = bf16lo(dw[i]), d1 = bf16hi(dw[i]);
-        dot = fmaf(d0, bf16lo(ow[i]), dot);
-        dot = fmaf(d1, bf16hi(ow[i]), dot);
-        out[i] = pack_bf16x2(g * d0, g * d1);
+    for (int j = 0; j < KT; ++j) {
+      rows[j] = __shfl_sync(0xffffffffu, my_row, j);
+      gs[j] = __shfl_sync(0xffffffffu, my_g, j);
+      dot[j] = 0.0f;
+    }
+    constexpr int U = KT <= 1 ? 8 : (KT <= 2 ? 4 : (KT <= 4 ? 2 : 1));
+    for (int v0 = lane; v0 < vec; v0 += 32 * U) {
+      uint4 dv[U], ov[U][KT];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + 32 * u;
+        if (v < vec) {
+          dv[u] = __ldg(dyr + v);
+#pragma unroll
+          for (int j = 0; j < KT; ++j)
+            if (rows[j] >= 0) ov[u][j] = __ldg(y_sorted + size_t(rows[j]) * vec + v);
+        }
       }
-      drow[v] = make_uint4(out[0], out[1], out[2], out[3]);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + 32 * u;
+        if (v >= vec) break;
+#pragma unroll
+        for (int j = 0; j < KT; ++j)
+          if (rows[j] >= 0)
+            d_o[size_t(rows[j]) * vec + v] = scale_dot_bf16x8(dv[u], ov[u][j], gs[j], dot[j]);
+        if (has_shared) shared_row[v] = dv[u];
+      }
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-    if (lane == 0) dgate[a] = dot;
-  }
-  if (has_shared) {
-    uint4* drow = d_o + size_t(R + t) * vec;
-    for (int v = lane; v < vec; v += 32) drow[v] = __ldg(dyr + v);
+    for (int j = 0; j < KT; ++j) {
+      float d = dot[j];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+      if (lane == 0) dgate[size_t(t) * KT + j] = rows[j] >= 0 ? d : 0.0f;
+    }
+  } else {
+    for (int j = 0; j < k; ++j) {
+      const int a = t * k + j;
+      const int row = __ldg(inv + a);
+      if (row < 0) {
+        if (lane == 0) dgate[a] = 0.0f;
+        continue;
+      }
+      const float g = __ldg(gate + a);
+      const uint4* orow = y_sorted + size_t(row) * vec;
+      uint4* drow = d_o + size_t(row) * vec;
+      float dot = 0.0f;
+      for (int v = lane; v < vec; v += 32) drow[v] = scale_dot_bf16x8(__ldg(dyr + v), __ldg(orow + v), g, dot);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+      if (lane == 0) dgate[a] = dot;
+    }
+    if (has_shared)
+      for (int v = lane; v < vec; v += 32) shared_row[v] = __ldg(dyr + v);
   }
 }
 
@@ -192,9 +242,21 @@ int launch_combine_backward(const moe_cfg& c, const void* dy, const void* y_sort
                             const int32_t* inv, const float* gate, void* d_o, float* dgate,
                             cudaStream_t st) {
   const int R = c.capacity ? c.E * c.capacity : c.T * c.k;
-  combine_backward_kernel<<<(c.T + 7) / 8, 256, 0, st>>>(
-      static_cast<const uint4*>(dy), static_cast<const uint4*>(y_sorted), inv, gate, c.T, c.k,
-      c.d / 8, R, c.has_shared, static_cast<uint4*>(d_o), dgate);
+  const uint4* dyv = static_cast<const uint4*>(dy);
+  const uint4* ys = static_cast<const uint4*>(y_sorted);
+  uint4* dov = static_cast<uint4*>(d_o);
+  const int blocks = (c.T + 7) / 8, vec = c.d / 8;
+#define MOE_CB(KTV) \
+  combine_backward_kernel<KTV><<<blocks, 256, 0, st>>>(dyv, ys, inv, gate, c.T, c.k, vec, R, \
+                                                      c.has_shared, dov, dgate)
+  switch (c.k) {
+    case 1: MOE_CB(1); break;
+    case 2: MOE_CB(2); break;
+    case 4: MOE_CB(4); break;
+    case 8: MOE_CB(8); break;
+    default: MOE_CB(0); break;
+  }
+#undef MOE_CB
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_E_CUDA;
 }
