@@ -38,12 +38,19 @@ __global__ void __launch_bounds__(256) fp8_pack_kernel(const uint4* __restrict__
   if (t >= T) return;
   const uint4* src = x + size_t(t) * vec_per_row;
   float amax = 0.0f;
-  for (int v = lane; v < vec_per_row; v += 32) {
-    const uint4 w = __ldg(src + v);
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+  constexpr int U = 4;  // vectors in flight per lane
+  for (int v0 = lane; v0 < vec_per_row; v0 += 32 * U) {
+    uint4 w[U];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      amax = fmaxf(amax, fmaxf(fabsf(bf16lo(u[i])), fabsf(bf16hi(u[i]))));
+    for (int q = 0; q < U; ++q)
+      w[q] = (v0 + 32 * q < vec_per_row) ? __ldg(src + v0 + 32 * q) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int q = 0; q < U; ++q) {
+      const uint32_t u[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        amax = fmaxf(amax, fmaxf(fabsf(bf16lo(u[i])), fabsf(bf16hi(u[i]))));
+    }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
@@ -108,19 +115,29 @@ __global__ void __launch_bounds__(256) fp8_recv_kernel(const uint4* __restrict__
     const float scale = __ldg(send_scale + p);
     const uint4* src = send_fp8 + size_t(p) * vec16_per_row;  // 16 codes per vector
     uint4* dst = x_sorted + size_t(row) * 2 * vec16_per_row;   // 8 bf16 per vector
-    for (int v = lane; v < vec16_per_row; v += 32) {
-      const uint4 c = __ldg(src + v);
-      uint4 o0, o1;
-      o0.x = deq2(c.x & 0xffffu, scale);
-      o0.y = deq2(c.x >> 16, scale);
-      o0.z = deq2(c.y & 0xffffu, scale);
-      o0.w = deq2(c.y >> 16, scale);
-      o1.x = deq2(c.z & 0xffffu, scale);
-      o1.y = deq2(c.z >> 16, scale);
-      o1.z = deq2(c.w & 0xffffu, scale);
-      o1.w = deq2(c.w >> 16, scale);
-      dst[2 * v] = o0;
-      dst[2 * v + 1] = o1;
+    // four code vectors in flight per lane, then their conversions
+    constexpr int U = 4;
+    for (int v0 = lane; v0 < vec16_per_row; v0 += 32 * U) {
+      uint4 c[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (v0 + 32 * u < vec16_per_row) c[u] = __ldg(src + v0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + 32 * u;
+        if (v >= vec16_per_row) break;
+        uint4 o0, o1;
+        o0.x = deq2(c[u].x & 0xffffu, scale);
+        o0.y = deq2(c[u].x >> 16, scale);
+        o0.z = deq2(c[u].y & 0xffffu, scale);
+        o0.w = deq2(c[u].y >> 16, scale);
+        o1.x = deq2(c[u].z & 0xffffu, scale);
+        o1.y = deq2(c[u].z >> 16, scale);
+        o1.z = deq2(c[u].w & 0xffffu, scale);
+        o1.w = deq2(c[u].w >> 16, scale);
+        dst[2 * v] = o0;
+        dst[2 * v + 1] = o1;
+      }
     }
   }
 }
