@@ -193,13 +193,17 @@ __device__ __forceinline__ void transpose_tile(const __nv_bfloat16* __restrict__
 // shared expert's T rows at src_shared) transposed into dst [C, ld_dst] at
 // columns [kpad_off[g], kpad_off[g+1]), zero past the kept rows.
 // grid.x: 64-column blocks of dst (up to the upper bound ld_dst / 64), grid.y:
-// 64-row blocks of C.
+// groups of kTrGroup 64-row blocks of C.  A CTA loads the next tile of its
+// group while it writes out the current one.
+constexpr int kTrGroup = 4;
+
 __global__ void __launch_bounds__(256) transpose_segments_kernel(
     const __nv_bfloat16* __restrict__ src, const __nv_bfloat16* __restrict__ src_shared, int C,
     const int32_t* __restrict__ offsets, const int32_t* __restrict__ counts, int capacity, int E,
     int has_shared, int T, const int32_t* __restrict__ kpad_off, __nv_bfloat16* __restrict__ dst,
     size_t ld_dst) {
   __shared__ uint32_t tile[kTr * (kTr / 2 + 1)];
+  constexpr int P = kTr / 2 + 1;
   const int n = E + has_shared;
   const int col = blockIdx.x * kTr;
   if (col >= __ldg(kpad_off + n)) return;
@@ -220,8 +224,54 @@ __global__ void __launch_bounds__(256) transpose_segments_kernel(
     kept = T;
     base = src_shared;
   }
-  transpose_tile(base + size_t(i0) * C, C, kept - i0, blockIdx.y * kTr, dst, ld_dst, size_t(col),
-                 tile);
+  base += size_t(i0) * C;
+  const int n_valid = kept - i0;  // source rows of this column block that exist
+  const int cb0 = blockIdx.y * kTrGroup, cb1 = min(C / kTr, cb0 + kTrGroup);
+  // this thread's two 16-byte vectors of a 64 x 64 tile: (row r, vector cv)
+  constexpr int PER = kTr * (kTr / 8) / 256;  // 2
+  uint4 buf[PER];
+  auto load = [&](int cb) {
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int i = threadIdx.x + q * 256;
+      const int r = i / (kTr / 8), cv = i % (kTr / 8);
+      buf[q] = r < n_valid
+                   ? __ldg(reinterpret_cast<const uint4*>(base + size_t(r) * C + cb * kTr) + cv)
+                   : make_uint4(0, 0, 0, 0);
+    }
+  };
+  load(cb0);
+  for (int cb = cb0; cb < cb1; ++cb) {
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int i = threadIdx.x + q * 256;
+      const int r = i / (kTr / 8), cv = i % (kTr / 8);
+      uint32_t* w = tile + r * P + cv * 4;
+      w[0] = buf[q].x;
+      w[1] = buf[q].y;
+      w[2] = buf[q].z;
+      w[3] = buf[q].w;
+    }
+    __syncthreads();
+    if (cb + 1 < cb1) load(cb + 1);  // in flight during the write-out below
+    const int c0 = cb * kTr;
+    for (int i = threadIdx.x; i < (kTr / 2) * (kTr / 8); i += blockDim.x) {
+      const int rv = i % (kTr / 8), c2 = i / (kTr / 8);  // rows 8rv..8rv+7, columns 2c2, 2c2+1
+      uint32_t lo4[4], hi4[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t a = tile[(rv * 8 + 2 * q) * P + c2];
+        const uint32_t b = tile[(rv * 8 + 2 * q + 1) * P + c2];
+        lo4[q] = (a & 0xffffu) | (b << 16);      // column 2c2 of rows 2q, 2q+1
+        hi4[q] = (a >> 16) | (b & 0xffff0000u);  // column 2c2+1
+      }
+      *reinterpret_cast<uint4*>(dst + size_t(c0 + 2 * c2) * ld_dst + col + rv * 8) =
+          make_uint4(lo4[0], lo4[1], lo4[2], lo4[3]);
+      *reinterpret_cast<uint4*>(dst + size_t(c0 + 2 * c2 + 1) * ld_dst + col + rv * 8) =
+          make_uint4(hi4[0], hi4[1], hi4[2], hi4[3]);
+    }
+    __syncthreads();
+  }
 }
 
 // Batched transpose of dense matrices: src [n][rows][cols] -> dst [n][cols][rows]
@@ -284,7 +334,7 @@ int launch_transpose_segments(const moe_cfg& c, const void* src, const void* src
                               const int32_t* offsets, const int32_t* counts,
                               const int32_t* kpad_off, void* dst, size_t ld_dst,
                               cudaStream_t st) {
-  const dim3 grid(unsigned(ld_dst / kTr), unsigned(C / kTr));
+  const dim3 grid(unsigned(ld_dst / kTr), unsigned((C / kTr + kTrGroup - 1) / kTrGroup));
   transpose_segments_kernel<<<grid, 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(src), static_cast<const __nv_bfloat16*>(src_shared), C,
       offsets, counts, c.capacity, c.E, c.has_shared, c.T, kpad_off,
