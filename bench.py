@@ -69,6 +69,16 @@ def _dist():
     return world, rank, local
 
 
+def _max_over_ranks(v, dev, world):
+    """The largest of every rank's value (each rank's own when world == 1): the
+    slowest replica sets the job's time."""
+    if world <= 1:
+        return float(v)
+    t = torch.tensor([float(v)], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 class _Clocks:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
 
@@ -411,10 +421,7 @@ def run_ours(args, cfg):
     per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(6)]
                     for i in range(args.steps)])  # ms
     step_ms = float(per.sum(1).mean())
-    if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = _max_over_ranks(step_ms, dev, world)
     status = m.moe_get_device_status(layer.ws)
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed steps")
@@ -451,10 +458,7 @@ def run_ours(args, cfg):
     e_ev.record(st)
     torch.cuda.synchronize(dev)
     e2e_ms = s_ev.elapsed_time(e_ev) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = _max_over_ranks(e2e_ms, dev, world)
 
     counts = layer.counts.cpu().numpy()
     alg = _algorithmic(cfg, counts, gather)
