@@ -106,7 +106,9 @@ int moe_pack_router(const moe_cfg* cfg, const float* W_r, moe_bf16* W_r_split, v
 /* Step 1, the router ("Expert parallelism", step 1 "Route": compute the
  * router for the local tokens).
  *   x          bf16 [T, d]
- *   W_r        fp32 [d, E], used when W_r_split is NULL (fp32 SIMT dot products)
+ *   W_r        fp32 [d, E], used when W_r_split is NULL: fp32 SIMT dot products
+ *              (E <= 16: W_r in registers, x streamed through a shared-memory
+ *              ring; larger E: 64 x 64 output tiles)
  *   W_r_split  bf16 [3, E, d] from moe_pack_router, or NULL.  When given, the
  *              logits come from the tensor cores: x times each of the three
  *              bf16 terms (every product exact in fp32), accumulated in fp32.
@@ -114,7 +116,8 @@ int moe_pack_router(const moe_cfg* cfg, const float* W_r, moe_bf16* W_r_split, v
  *   scores     fp32 [T, E] out: logits l = x W_r (+ logit_bias), fp32
  *              accumulation; with MOE_SIGMOID the affinity 1/(1+exp(-l)).
  *   ws         workspace or NULL: receives MOE_E_DEVICE_TIMEOUT if a bounded
- *              wait of the tensor-core path gives up. */
+ *              wait (tensor-core path, or the E <= 16 ring) gives up; the
+ *              block that gave up writes no scores. */
 int moe_router_logits(const moe_cfg* cfg, const moe_bf16* x, const float* W_r,
                       const moe_bf16* W_r_split, const float* logit_bias, float* scores,
                       void* ws, size_t ws_bytes, void* stream);
