@@ -55,6 +55,9 @@ struct GroupedParams {
   int K;                  // reduction length of one pass
   int k_passes;           // passes over K: A re-read each pass, B advanced by b_pass_rows
   int b_pass_rows;
+  int merge_passes;       // 1 (with the kernel's kMerge): one pass over K; each k-block loads
+                          //   A once and the k_passes B boxes side by side, and multiplies
+                          //   A by each of them
   int N;                  // weight rows per expert (output columns before SwiGLU)
   int mode;               // kEpiSwiglu: out[:, j] = silu(acc[:, gate j]) * acc[:, up j]
                           // kEpiBf16:   out = bf16(acc)
@@ -144,6 +147,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Gr
 
 // tmA / tmA_sh: 128-row A boxes; tmA64 / tmA_sh64: the same tensors with 64-row
 // boxes for half tiles.
+template <bool kMerge>
 __global__ void __launch_bounds__(gg::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmA_sh,
@@ -163,7 +167,8 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
   const int n_blocks_n = (p.N + NM - 1) / NM;
   const bool wgrad = p.kpad_off != nullptr;
   const int kb_per_pass = wgrad ? (1 << 30) : p.K / BK;
-  const int num_kb = wgrad ? 0 : kb_per_pass * p.k_passes;
+  const int n_b = kMerge ? p.k_passes : 1;  // B boxes per stage
+  const int num_kb = wgrad ? 0 : (kMerge ? kb_per_pass : kb_per_pass * p.k_passes);
   // first column and k-blocks of segment g's reduction
   auto tile_k = [&](int g, int& k0, int& nkb) {
     if (wgrad) {
@@ -273,7 +278,7 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
           const bool sep = p.counts && g >= p.E && p.shared_a_separate;
           const bool half = is_half(rows, m_blk);
           const CUtensorMap* ma = half ? (sep ? &tmA_sh64 : &tmA64) : (sep ? &tmA_sh : &tmA);
-          const uint32_t tx = (half ? A_BYTES / 2 : A_BYTES) + b_bytes;
+          const uint32_t tx = (half ? A_BYTES / 2 : A_BYTES) + n_b * b_bytes;
           const int a_row = a_row0 + m_blk * BM;
           const int b_row = (wgrad ? 0 : g * p.N) + n_blk * NM;
           int k0, nkb;
@@ -285,7 +290,13 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
             const int ka = k0 + (kb - pass * kb_per_pass) * BK;
             mbar_arrive_expect_tx(&ctl.full[stage], tx);
             tma_load_2d(sa, ma, ka, a_row, &ctl.full[stage]);
-            tma_load_2d(sa + A_BYTES, &tmB, ka, b_row + pass * p.b_pass_rows, &ctl.full[stage]);
+            if (!kMerge) {
+              tma_load_2d(sa + A_BYTES, &tmB, ka, b_row + pass * p.b_pass_rows, &ctl.full[stage]);
+            } else {
+              for (int j = 0; j < n_b; ++j)
+                tma_load_2d(sa + A_BYTES + j * b_bytes, &tmB, ka, b_row + j * p.b_pass_rows,
+                            &ctl.full[stage]);
+            }
             issued |= 1u << stage;
             last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -374,10 +385,12 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
           tc_fence_after();
           const uint8_t* sa = smem + stage * STAGE_BYTES;
           const uint64_t a_desc = smem_desc_k128(sa);
-          const uint64_t b_desc = smem_desc_k128(sa + A_BYTES);
+          for (int j = 0; j < n_b; ++j) {
+            const uint64_t b_desc = smem_desc_k128(sa + A_BYTES + j * b_bytes);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            umma_bf16(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc, (kb | kk) != 0);
+            for (int kk = 0; kk < BK / 16; ++kk)
+              umma_bf16(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc, (kb | kk | j) != 0);
+          }
           umma_commit(&ctl.empty[stage]);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -641,8 +654,11 @@ static int set_smem_attr() {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    err = cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               int(gg::DYN_SMEM));
+    err = cudaFuncSetAttribute(grouped_gemm_kernel<false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, int(gg::DYN_SMEM));
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(grouped_gemm_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(gg::DYN_SMEM));
   });
   return err == cudaSuccess ? MOE_OK : MOE_E_CUDA;
 }
@@ -661,7 +677,8 @@ static int launch_gg(int64_t rows_ub, int n_seg, const CUtensorMap& a, const CUt
   const int sms = device_sm_count();
   const long long tiles = (rows_ub / gg::BM + n_seg) * ((p.N + gg::BN - 1) / gg::BN);
   const int grid = int(tiles < sms ? tiles : sms);
-  grouped_gemm_kernel<<<grid, gg::THREADS, gg::DYN_SMEM, st>>>(a, a_sh, a64, a_sh64, b, out, p);
+  grouped_gemm_kernel<false><<<grid, gg::THREADS, gg::DYN_SMEM, st>>>(a, a_sh, a64, a_sh64, b,
+                                                                     out, p);
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_E_CUDA;
 }
@@ -706,6 +723,9 @@ int launch_router_tc(const moe_cfg& c, const void* x, const void* W_split, const
   p.K = c.d;
   p.k_passes = 3;
   p.b_pass_rows = c.E;
+  // the three B boxes of a k-block fit the stage's B slot together up to 80
+  // columns: then A is read once instead of once per term
+  p.merge_passes = 3u * uint32_t(nm) * BK * 2 <= B_BYTES ? 1 : 0;
   p.N = c.E;
   p.mode = kEpiF32;
   p.out_f32 = out;
@@ -716,7 +736,10 @@ int launch_router_tc(const moe_cfg& c, const void* x, const void* W_split, const
   p.n_mma = nm;
   const long long tiles = (long long)((c.T + BM - 1) / BM) * ((c.E + BN - 1) / BN);
   const int grid = int(tiles < sms ? tiles : sms);
-  grouped_gemm_kernel<<<grid, THREADS, DYN_SMEM, st>>>(mA, mA, mA64, mA64, mB, mB, p);
+  if (p.merge_passes)
+    grouped_gemm_kernel<true><<<grid, THREADS, DYN_SMEM, st>>>(mA, mA, mA64, mA64, mB, mB, p);
+  else
+    grouped_gemm_kernel<false><<<grid, THREADS, DYN_SMEM, st>>>(mA, mA, mA64, mA64, mB, mB, p);
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_E_CUDA;
 }
@@ -810,7 +833,8 @@ int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
 
   const long long t1 = mt_ub * ((p1.N + BN - 1) / BN);
   const int grid1 = int(t1 < sms ? t1 : sms);
-  grouped_gemm_kernel<<<grid1, THREADS, DYN_SMEM, st>>>(mA1, mA1s, mA1h, mA1sh, mB1, mB1, p1);
+  grouped_gemm_kernel<false><<<grid1, THREADS, DYN_SMEM, st>>>(mA1, mA1s, mA1h, mA1sh, mB1, mB1,
+                                                               p1);
 
   GroupedParams p2 = p1;
   p2.gather_order = nullptr;
@@ -826,7 +850,7 @@ int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
   CUtensorMap mOut2;
   if (!make_map(&mOut2, y_sorted, rows_h, c.d, 32)) return MOE_E_CUDA;
   p2.tma_store = 1;
-  grouped_gemm_kernel<<<grid2, THREADS, DYN_SMEM, st>>>(mA2, mA2, mA2h, mA2h, mB2, mOut2, p2);
+  grouped_gemm_kernel<false><<<grid2, THREADS, DYN_SMEM, st>>>(mA2, mA2, mA2h, mA2h, mB2, mOut2, p2);
   note_launches(2);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_E_CUDA;
 }
