@@ -20,15 +20,31 @@ namespace moe {
 //   chunk_hist     int32 [n_chunks][E] per-chunk histogram, then chunk bases
 //   ep_sbase       int32 [n_ep][E]   (unused: the layout kernel keeps these bases in shared memory)
 //   send_pos       int32 [A]         send slot of each assignment (-1 dropped)
+//   router_part    fp32 [S][T][E]    partial logits of the tensor-core router when it
+//                                    splits K into S > 1 chunks (router_k_split)
 // ---------------------------------------------------------------------------
 constexpr int kPermChunk = 2048;   // assignments per histogram/rank CTA
 
 struct WsLayout {
-  size_t status, done_ctas, src_cnt, chunk_hist, ep_sbase, send_pos, total;
+  size_t status, done_ctas, src_cnt, chunk_hist, ep_sbase, send_pos, router_part, total;
   int n_chunks;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// K chunks of the tensor-core router.  Its 128 x 256 output tiles are few when
+// T is small (one tile for a 128-token decode batch), so K is split into S
+// chunks reduced afterwards in a fixed order: S is the largest divisor of d/64
+// that keeps at least 8 k-blocks per chunk and at most 148 tiles in all (one
+// wave on a B300).  A rule of the shape alone, so the workspace size is too.
+inline int router_k_split(const moe_cfg& c) {
+  const long long tiles = (long long)((c.T + 127) / 128) * ((c.E + 255) / 256);
+  const int kb = c.d / 64;
+  int best = 1;
+  for (int s = 2; s <= kb / 8; ++s)
+    if (kb % s == 0 && tiles * s <= 148) best = s;
+  return best;
+}
 
 inline WsLayout ws_layout(const moe_cfg& c) {
   WsLayout L;
@@ -40,6 +56,9 @@ inline WsLayout ws_layout(const moe_cfg& c) {
   L.chunk_hist = off; off += align256(size_t(L.n_chunks) * c.E * 4);
   L.ep_sbase = off;   off += align256(size_t(c.n_ep) * c.E * 4);
   L.send_pos = off;   off += align256(A * 4);
+  const int ks = router_k_split(c);
+  L.router_part = off;
+  if (ks > 1) off += align256(size_t(ks) * c.T * c.E * 4);
   L.total = off;
   return L;
 }

@@ -55,6 +55,8 @@ struct GroupedParams {
   int K;                  // reduction length of one pass
   int k_passes;           // passes over K: A re-read each pass, B advanced by b_pass_rows
   int b_pass_rows;
+  int k_split;            // dense mode: > 1 = segment g reduces K chunk g (length K) into
+                          //   its own partial output rows [g*dense_rows, (g+1)*dense_rows)
   int merge_passes;       // 1 (with the kernel's kMerge): one pass over K; each k-block loads
                           //   A once and the k_passes B boxes side by side, and multiplies
                           //   A by each of them
@@ -115,7 +117,7 @@ __device__ __forceinline__ void segment(const GroupedParams& p, int g, int& rows
   } else if (p.counts == nullptr) {
     rows = p.dense_rows;
     a_row0 = 0;
-    out_row0 = 0;
+    out_row0 = g * p.dense_rows;  // g > 0 only with k_split
   } else if (g < p.E) {
     const int c = __ldg(p.counts + g);
     rows = p.capacity ? min(c, p.capacity) : c;
@@ -161,7 +163,7 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) &
                                              ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_seg = p.counts ? p.E + p.has_shared : 1;
+  const int n_seg = p.counts ? p.E + p.has_shared : (p.k_split > 1 ? p.k_split : 1);
   const int NM = p.n_mma ? p.n_mma : BN;                // tile width
   const uint32_t b_bytes = uint32_t(NM) * BK * 2;
   const int n_blocks_n = (p.N + NM - 1) / NM;
@@ -175,7 +177,7 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
       k0 = __ldg(p.kpad_off + g);
       nkb = (__ldg(p.kpad_off + g + 1) - k0) / BK;
     } else {
-      k0 = 0;
+      k0 = p.counts == nullptr && p.k_split > 1 ? g * p.K : 0;
       nkb = num_kb;
     }
   };
@@ -280,7 +282,8 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
           const CUtensorMap* ma = half ? (sep ? &tmA_sh64 : &tmA64) : (sep ? &tmA_sh : &tmA);
           const uint32_t tx = (half ? A_BYTES / 2 : A_BYTES) + n_b * b_bytes;
           const int a_row = a_row0 + m_blk * BM;
-          const int b_row = (wgrad ? 0 : g * p.N) + n_blk * NM;
+          // per-segment weights (grouped mode); one shared B otherwise
+          const int b_row = (wgrad || p.counts == nullptr ? 0 : g * p.N) + n_blk * NM;
           int k0, nkb;
           tile_k(g, k0, nkb);
           for (int kb = 0; kb < nkb; ++kb) {
@@ -704,8 +707,24 @@ int launch_pack_w13(const moe_cfg& c, const void* W1, const void* W3, void* W13,
 // Router logits on the tensor cores: x [T, d] (bf16) times the three bf16
 // terms of W_r (W_r = hi + mid + lo exactly, stored [3][E][d]), accumulated in
 // fp32 in tensor memory over 3 passes of K, + logit bias, sigmoid if asked.
+// Fixed-order sum of the router's K-chunk partials, + logit bias, sigmoid if
+// asked: out[t][e] = sum over s of part[s][t][e].
+__global__ void __launch_bounds__(256) router_split_reduce_kernel(
+    const float* __restrict__ part, int S, int T, int E, const float* __restrict__ lbias,
+    int sigmoid, float* __restrict__ out) {
+  const size_t n = size_t(T) * E;
+  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += size_t(gridDim.x) * blockDim.x) {
+    float l = 0.0f;
+    for (int s = 0; s < S; ++s) l += __ldg(part + size_t(s) * n + i);
+    if (lbias) l += __ldg(lbias + i % E);
+    if (sigmoid) l = 1.0f / (1.0f + expf(-l));
+    out[i] = l;
+  }
+}
+
 int launch_router_tc(const moe_cfg& c, const void* x, const void* W_split, const float* lbias,
-                     float* out, int* status, cudaStream_t st) {
+                     float* out, int* status, float* part, cudaStream_t st) {
   using namespace gg;
   if (!get_encoder()) return MOE_E_CUDA;
   if (set_smem_attr() != MOE_OK) return MOE_E_CUDA;
@@ -734,13 +753,29 @@ int launch_router_tc(const moe_cfg& c, const void* x, const void* W_split, const
   p.ld_out = c.E;
   p.status = status;
   p.n_mma = nm;
-  const long long tiles = (long long)((c.T + BM - 1) / BM) * ((c.E + BN - 1) / BN);
+  // split K when the output tiles are few (and a partial buffer is given)
+  const int ks = part ? router_k_split(c) : 1;
+  if (ks > 1) {
+    p.k_split = ks;
+    p.K = c.d / ks;
+    p.out_f32 = part;
+    p.col_bias = nullptr;
+    p.sigmoid = 0;
+  }
+  const long long tiles = (long long)((c.T + BM - 1) / BM) * ((c.E + BN - 1) / BN) * ks;
   const int grid = int(tiles < sms ? tiles : sms);
   if (p.merge_passes)
     grouped_gemm_kernel<true><<<grid, THREADS, DYN_SMEM, st>>>(mA, mA, mA64, mA64, mB, mB, p);
   else
     grouped_gemm_kernel<false><<<grid, THREADS, DYN_SMEM, st>>>(mA, mA, mA64, mA64, mB, mB, p);
   note_launches(1);
+  if (ks > 1) {
+    const long long n = (long long)c.T * c.E;
+    const int blocks = int((n + 255) / 256 < 4 * sms ? (n + 255) / 256 : 4 * sms);
+    router_split_reduce_kernel<<<blocks, 256, 0, st>>>(part, ks, c.T, c.E, lbias,
+                                                       c.score_fn == MOE_SIGMOID, out);
+    note_launches(1);
+  }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_E_CUDA;
 }
 

@@ -19,7 +19,7 @@ int device_sm_count();
 int launch_router_logits(const moe_cfg& c, const void* x, const float* W, const float* lbias,
                          float* out, int* status, cudaStream_t st);
 int launch_router_tc(const moe_cfg& c, const void* x, const void* W_split, const float* lbias,
-                     float* out, int* status, cudaStream_t st);
+                     float* out, int* status, float* part, cudaStream_t st);
 int launch_pack_router(const moe_cfg& c, const float* W, void* out, cudaStream_t st);
 int launch_route(const moe_cfg& c, const float* scores, const float* bias, int32_t* idx,
                  float* gate, cudaStream_t st);

@@ -151,7 +151,8 @@ MOE_API int moe_router_logits(const moe_cfg* c, const moe_bf16* x, const float* 
   MOE_TRY(device_ok());
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* status = ws ? ws_ptr<int>(ws, ws_layout(*c).status) : nullptr;
-  if (W_r_split) return launch_router_tc(*c, x, W_r_split, logit_bias, scores, status, st);
+  float* part = ws ? ws_ptr<float>(ws, ws_layout(*c).router_part) : nullptr;
+  if (W_r_split) return launch_router_tc(*c, x, W_r_split, logit_bias, scores, status, part, st);
   return launch_router_logits(*c, x, W_r, logit_bias, scores, status, st);
 }
 

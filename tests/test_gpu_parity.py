@@ -308,6 +308,42 @@ def test_router_logits_simt_shapes(m, E, d, T, sig):
         assert (np.abs(got - l_ref) <= bound).all()
 
 
+@pytest.mark.parametrize("E,d,T,sig", [(256, 2048, 64, True), (64, 1024, 300, False),
+                                       (256, 7168, 128, True), (32, 4096, 129, False)])
+def test_router_tc_split_k(m, E, d, T, sig):
+    """The tensor-core router with its K split into chunks (few output tiles:
+    decode-sized batches) and the fixed-order reduction of the partials, with
+    logit bias and sigmoid; against fp64 within the three-term bound.  The
+    same call without a workspace takes the unsplit path; both must agree
+    within twice the bound."""
+    g = torch.Generator().manual_seed(E + d + T)
+    cfg = C["dsv3"].with_(T=T, d=d, E=E, k=8, n_groups=1, topk_groups=1, n_ep=1,
+                          score_fn="sigmoid" if sig else "softmax", norm_topk=int(sig),
+                          has_shared=0)
+    c = m.MoeCfg.from_layer(cfg)
+    x = torch.randn(T, d, generator=g).bfloat16()
+    W_r = (torch.randn(d, E, generator=g) / math.sqrt(d)).float()
+    lb = (torch.randn(E, generator=g) * 0.5).float()
+    split = _router_split(m, c, W_r.cuda())
+    ws = torch.zeros(m.moe_workspace_bytes(c), dtype=torch.uint8, device="cuda")
+    m.moe_workspace_init(c, ws)
+    out = torch.full((T, E), float("nan"), dtype=torch.float32, device="cuda")
+    out1 = torch.full((T, E), float("nan"), dtype=torch.float32, device="cuda")
+    m.moe_router_logits(c, x.cuda(), None, split, lb.cuda(), out, ws)
+    m.moe_router_logits(c, x.cuda(), None, split, lb.cuda(), out1)
+    torch.cuda.synchronize()
+    assert m.moe_get_device_status(ws) == 0
+    xf, Wf = x.float().numpy(), W_r.numpy()
+    l_ref = oracle.router_logits(xf, Wf, lb.numpy())
+    bound = 3 * _logit_bound(xf, Wf) + 2.0 ** -24 * np.abs(l_ref) + 1e-30
+    got, got1 = npf(out), npf(out1)
+    assert np.isfinite(got).all() and np.isfinite(got1).all()
+    ref = oracle.sigmoid(l_ref) if sig else l_ref
+    scale = 0.25 if sig else 1.0
+    assert (np.abs(got - ref) <= scale * bound + (4e-7 if sig else 0.0)).all()
+    assert (np.abs(got - got1) <= 2 * scale * bound + (8e-7 if sig else 0.0)).all()
+
+
 def test_router_split_is_exact(m):
     """hi + mid + lo reproduces every fp32 router weight exactly."""
     cfg = SMALL["ds_small"]
