@@ -115,9 +115,12 @@ int moe_pack_router(const moe_cfg* cfg, const float* W_r, moe_bf16* W_r_split, v
  *   logit_bias fp32 [E] or NULL: added to every token's logits
  *   scores     fp32 [T, E] out: logits l = x W_r (+ logit_bias), fp32
  *              accumulation; with MOE_SIGMOID the affinity 1/(1+exp(-l)).
- *   ws         workspace or NULL: receives MOE_E_DEVICE_TIMEOUT if a bounded
- *              wait (tensor-core path, or the E <= 16 ring) gives up; the
- *              block that gave up writes no scores. */
+ *   ws         workspace or NULL.  With a workspace, the tensor-core path splits
+ *              K into chunks when its 128 x 256 output tiles are few (small T)
+ *              and keeps the partial logits there, summed afterwards in a fixed
+ *              order.  It receives MOE_E_DEVICE_TIMEOUT if a bounded wait
+ *              (tensor-core path, or the E <= 16 ring) gives up; the block that
+ *              gave up writes no scores. */
 int moe_router_logits(const moe_cfg* cfg, const moe_bf16* x, const float* W_r,
                       const moe_bf16* W_r_split, const float* logit_bias, float* scores,
                       void* ws, size_t ws_bytes, void* stream);
