@@ -177,12 +177,8 @@ class MoELayer:
         wait for the last result)."""
         comp = torch.cuda.current_stream(self.device)
         s_in, s_out = self._copy_streams()
-        T, d = self.cfg.T, self.cfg.d
-        if getattr(self, "_xbuf", None) is None:
-            self._xbuf = [torch.empty(T, d, dtype=torch.bfloat16, device=self.device)
-                          for _ in range(2)]
-            self._ybuf = [torch.empty(T, d, dtype=torch.bfloat16, device=self.device)
-                          for _ in range(2)]
+        self._stream_buffers()
+        graphs = getattr(self, "_graphs", None)
         ev = lambda: torch.cuda.Event()  # noqa: E731
         in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
         start = ev()
@@ -198,7 +194,10 @@ class MoELayer:
             comp.wait_event(in_done[b])
             if i >= 2:
                 comp.wait_event(out_done[b])      # batch i-2's result has left ybuf[b]
-            self.forward(self._xbuf[b], y=self._ybuf[b])
+            if graphs:
+                graphs[b].replay()
+            else:
+                self.forward(self._xbuf[b], y=self._ybuf[b])
             comp_done[b].record(comp)
             s_out.wait_event(comp_done[b])
             with torch.cuda.stream(s_out):
@@ -208,6 +207,38 @@ class MoELayer:
         for b in range(min(n, 2)):
             comp.wait_event(out_done[b])
         return y_hosts
+
+    def capture_graphs(self):
+        """Records the forward on each of forward_host_stream's two device
+        buffer pairs as a CUDA graph, after one eager call per pair (one-time
+        set-up such as kernel attributes happens there).  forward_host_stream
+        then replays one graph per batch instead of issuing about ten calls,
+        which matters when a batch computes in less time than the host takes
+        to issue it.  The graphs hold this layer's buffers and workspace; call
+        again after changing the layer's weights' storage."""
+        self._stream_buffers()
+        self._graphs = None
+        comp = torch.cuda.current_stream(self.device)
+        for b in range(2):
+            self.forward(self._xbuf[b], y=self._ybuf[b])
+        torch.cuda.synchronize(self.device)
+        graphs = []
+        for b in range(2):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.forward(self._xbuf[b], y=self._ybuf[b])
+            graphs.append(g)
+        comp.synchronize()
+        self._graphs = graphs
+        return graphs
+
+    def _stream_buffers(self):
+        if getattr(self, "_xbuf", None) is None:
+            T, d = self.cfg.T, self.cfg.d
+            self._xbuf = [torch.empty(T, d, dtype=torch.bfloat16, device=self.device)
+                          for _ in range(2)]
+            self._ybuf = [torch.empty(T, d, dtype=torch.bfloat16, device=self.device)
+                          for _ in range(2)]
 
     def _copy_streams(self):
         if getattr(self, "_streams", None) is None:

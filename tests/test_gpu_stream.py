@@ -1,7 +1,8 @@
 """The streaming host call: several host batches through
 MoELayer.forward_host_stream (copies on their own streams, overlapping
-compute, two device buffers per side) give, batch for batch, exactly the
-outputs of the plain device forward."""
+compute, two device buffers per side), with the forward issued call by call
+or replayed from CUDA graphs, give, batch for batch, exactly the outputs of
+the plain device forward."""
 import pytest
 import torch
 
@@ -10,8 +11,9 @@ import synth
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("name,n", [("tiny", 5), ("mixtral", 3)])
-def test_forward_host_stream_matches_device_forward(name, n):
+@pytest.mark.parametrize("graphs", [False, True])
+@pytest.mark.parametrize("name,n", [("tiny", 5), ("mixtral", 3), ("dsv3_decode", 3)])
+def test_forward_host_stream_matches_device_forward(name, n, graphs):
     import expert_token_dispatch_moe_b300 as m
     cfg = synth.CONFIGS[name]
     if name == "mixtral":
@@ -19,6 +21,8 @@ def test_forward_host_stream_matches_device_forward(name, n):
     W1, W3, W2 = synth.make_expert_weights(cfg, device="cuda")
     W_r, lb = synth.make_router(cfg, device="cuda")
     layer = m.MoELayer(cfg, W1, W3, W2, W_r=W_r, logit_bias=lb)
+    if graphs:
+        layer.capture_graphs()
     xs = [synth.make_x(cfg, seed=100 + i).pin_memory() for i in range(n)]
     ys = [torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory() for _ in range(n)]
     layer.forward_host_stream(xs, ys)
