@@ -1,0 +1,92 @@
+"""Property checks of the oracle's permutation and expert-parallel layout over
+random small configurations (hypothesis).  Each property is checked by direct
+counting with plain loops, not by the oracle's own numpy route (argsort,
+bincount, lexsort): per expert, the kept assignments are the first ones in
+increasing a and sit in consecutive rows from the segment's start; every row
+and every send slot is accounted for exactly once; the count matrix's row
+and column sums are the rows each rank sends and receives."""
+import numpy as np
+from hypothesis import given, settings
+from hypothesis import strategies as st
+
+import oracle
+
+
+@st.composite
+def routing(draw):
+    n_ep = draw(st.sampled_from([1, 2, 4]))
+    E = n_ep * draw(st.integers(1, 4))
+    k = draw(st.integers(1, min(E, 3)))
+    T = n_ep * draw(st.integers(1, 6))
+    rows = []
+    for _ in range(T):
+        rows.append(draw(st.permutations(list(range(E))))[:k])
+    cap = draw(st.sampled_from([0, 0, 1, 2, 3]))
+    return np.array(rows, dtype=np.int64).reshape(T, k), E, n_ep, cap
+
+
+@settings(max_examples=150, deadline=None)
+@given(routing())
+def test_permute_properties(case):
+    idx, E, n_ep, cap = case
+    T, k = idx.shape
+    A = T * k
+    flat = [int(v) for v in idx.reshape(-1)]
+    p = oracle.permute(idx, E, cap)
+    inv, order, counts, offsets = p["inv"], p["order"], p["counts"], p["offsets"]
+    R = E * cap if cap else A
+    assert order.shape == (R,) and inv.shape == (A,)
+    start = 0
+    for e in range(E):
+        mine = [a for a in range(A) if flat[a] == e]          # increasing a
+        assert counts[e] == len(mine)
+        seg = e * cap if cap else start
+        assert offsets[e] == seg
+        kept = mine[:cap] if cap else mine
+        for r, a in enumerate(kept):                          # consecutive rows, stable
+            assert inv[a] == seg + r and order[seg + r] == a
+        for a in mine[len(kept):]:                            # dropped overflow
+            assert inv[a] == -1
+        if cap:
+            for r in range(len(kept), cap):                   # padding rows
+                assert order[seg + r] == -1
+        start += len(mine)
+    assert offsets[E] == (E * cap if cap else A)
+    # every row holds at most one assignment and every kept assignment one row
+    rows_used = [r for r in range(R) if order[r] >= 0]
+    assert sorted(inv[inv >= 0].tolist()) == rows_used
+
+
+@settings(max_examples=150, deadline=None)
+@given(routing())
+def test_ep_layout_properties(case):
+    idx, E, n_ep, cap = case
+    T, k = idx.shape
+    A, T_loc = T * k, T // n_ep
+    p = oracle.permute(idx, E, cap)
+    lay = oracle.ep_layout(idx, p["inv"], E, n_ep, T)
+    C, send_off, recv_off, send_idx = lay["C"], lay["send_off"], lay["recv_off"], lay["send_idx"]
+    flat = [int(v) for v in idx.reshape(-1)]
+    inv = p["inv"]
+    rank_of = [e * n_ep // E for e in range(E)]
+    for s in range(n_ep):
+        lo, hi = s * T_loc * k, (s + 1) * T_loc * k
+        kept = [a for a in range(lo, hi) if inv[a] >= 0]
+        # the rank's slots: its kept assignments by (destination, expert, a), then -1
+        want = sorted(kept, key=lambda a: (rank_of[flat[a]], flat[a], a))
+        assert send_idx[lo:lo + len(want)].tolist() == want
+        assert (send_idx[lo + len(want):hi] == -1).all()
+        run = 0
+        for q in range(n_ep):
+            c = sum(1 for a in kept if rank_of[flat[a]] == q)
+            assert C[s, q] == c
+            assert send_off[s, q] == run
+            run += c
+        assert C[s].sum() == len(kept)                        # row sum: rows s sends
+    for q in range(n_ep):
+        received = sum(1 for a in range(A) if inv[a] >= 0 and rank_of[flat[a]] == q)
+        assert C[:, q].sum() == received                      # column sum: rows q receives
+        run = 0
+        for s in range(n_ep):
+            assert recv_off[q, s] == run
+            run += C[s, q]
