@@ -26,6 +26,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -89,7 +90,9 @@ class _Clocks:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        # raw samples: MOE_BENCH_CLOCKS_DIR if set, else the temp directory
+        base = os.environ.get("MOE_BENCH_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(base, f"moe_bench_clocks_rank{index}.csv")
 
     def start(self):
         try:
