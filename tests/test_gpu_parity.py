@@ -174,8 +174,9 @@ def test_hot_expert_capacity_drops(m):
     _check_permute(cfg, x_dev, idx_np, out, lay)
 
 
-def test_bad_expert_id_is_reported(m):
-    cfg = C["tiny"].with_(T=64, E=8, k=2, n_ep=2, d=64)
+@pytest.mark.parametrize("T", [64, 2500])   # one-CTA index kernel, and the multi-CTA path
+def test_bad_expert_id_is_reported(m, T):
+    cfg = C["tiny"].with_(T=T, E=8, k=2, n_ep=2, d=64)
     c = m.MoeCfg.from_layer(cfg)
     idx = torch.zeros(cfg.T, cfg.k, dtype=torch.int32)
     idx[:, 1] = 1
