@@ -102,3 +102,28 @@ def test_host_argument_errors(m):
         assert lib.moe_selftest_wait_timeout(P, 10 ** 6, None) == -6
     for code in range(-8, 1):
         assert lib.moe_strerror(code)
+
+
+def _k_split(T, E, d):
+    """The router's K-split rule restated: the largest divisor S of d/64 with at
+    least 8 k-blocks per chunk and at most 148 output tiles in all."""
+    tiles = ((T + 127) // 128) * ((E + 255) // 256)
+    kb = d // 64
+    return max([s for s in range(1, kb // 8 + 1) if kb % s == 0 and tiles * s <= 148] or [1])
+
+
+def test_workspace_holds_router_k_split_partials(m):
+    """The workspace grows by exactly S*T*E fp32 partial logits (256-byte
+    aligned) when the tensor-core router splits K, and not at all otherwise."""
+    def align(x):
+        return (x + 255) // 256 * 256
+    for name, kw in [("dsv3_decode", {}), ("dsv3", {}), ("dsv3", {"T": 64, "d": 2048}),
+                     ("mixtral", {}), ("skew", {}), ("tiny", {})]:
+        cfg = synth.CONFIGS[name].with_(**kw)
+        c = m.MoeCfg.from_layer(cfg)
+        S = _k_split(cfg.T, cfg.E, cfg.d)
+        base = m.moe_workspace_bytes(m.MoeCfg.from_layer(cfg.with_(d=64)))  # d/64 = 1: never splits
+        extra = m.moe_workspace_bytes(c) - base
+        assert extra == (align(S * cfg.T * cfg.E * 4) if S > 1 else 0), (name, kw, S)
+    assert _k_split(128, 256, 7168) == 14 and _k_split(8192, 256, 7168) == 2
+
