@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(1024) eplb_plan_kernel(
     double* __restrict__ rank_load) {
   __shared__ int c_sm[1024], q_sm[1024], sorted_sm[1024], off_sm[1024];
   __shared__ int used_sm[1024];
-  __shared__ double load_sm[1024];
+  __shared__ double load_sm[1024], per_sm[1024];
   __shared__ int warp_tot[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int i = tid; i < E; i += blockDim.x) {
@@ -130,23 +130,28 @@ __global__ void __launch_bounds__(1024) eplb_plan_kernel(
   }
   __syncthreads();
 
-  // 2c. Pack: one warp places the copies in order.
+  // 2c. Pack: one warp places the copies in order.  Each copy's load (one
+  // fp64 division per expert) is computed up front, in parallel; rank loads
+  // are sums of non-negative doubles, so their order is the order of their
+  // bit patterns as integers (no fp64 compares on the critical path).
+  for (int i = tid; i < E; i += blockDim.x) per_sm[i] = double(c_sm[i]) / double(q_sm[i]);
+  __syncthreads();
   if (warp == 0) {
     for (int p = 0; p < E; ++p) {
       const int i = sorted_sm[p];
-      const double per = double(c_sm[i]) / double(q_sm[i]);
+      const double per = per_sm[i];
       for (int j = 0; j < q_sm[i]; ++j) {
         int br = -1;
-        double bl = 0.0;
+        long long bl = 0;
         for (int r = lane; r < n_ranks; r += 32) {
           if (used_sm[r] >= slots) continue;
-          const double l = load_sm[r];
+          const long long l = __double_as_longlong(load_sm[r]);
           if (br < 0 || l < bl) { br = r; bl = l; }   // ranks ascend per lane
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
           const int orr = __shfl_xor_sync(0xffffffffu, br, off);
-          const double ol = __shfl_xor_sync(0xffffffffu, bl, off);
+          const long long ol = __shfl_xor_sync(0xffffffffu, bl, off);
           if (orr >= 0 && (br < 0 || ol < bl || (ol == bl && orr < br))) { br = orr; bl = ol; }
         }
         if (lane == 0) {
