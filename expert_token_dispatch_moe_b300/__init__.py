@@ -308,6 +308,10 @@ def moe_get_device_status(ws, stream=None) -> int:
     return _lib.moe_get_device_status(_ptr(ws), _stream(stream))
 
 
+def moe_strerror(code) -> str:
+    return _lib.moe_strerror(int(code)).decode()
+
+
 def moe_last_launch_count() -> int:
     return _lib.moe_last_launch_count()
 

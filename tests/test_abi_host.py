@@ -35,6 +35,11 @@ def test_header_declares_what_library_exports(m):
     assert exported == declared
 
 
+def test_every_entry_point_has_a_wrapper(m):
+    assert [n for n in m.EXPORTS if not callable(getattr(m, n, None))] == []
+    assert m.moe_strerror(-8) == "a device-side wait timed out"
+
+
 def test_validate_cfg_limits(m):
     ok = m.MoeCfg.from_layer(synth.CONFIGS["dsv3"])
     assert m.moe_validate_cfg(ok) == 0
