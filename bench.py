@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -81,20 +82,46 @@ def _max_over_ranks(v, dev, world):
 
 
 class _Clocks:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    """SM clocks and throttle reasons during the timed region: NVML read every
+    20 ms from a thread (the statistics), and nvidia-smi every 200 ms beside it
+    (the raw record, kept as a file)."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clocks-event reason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.thread = None
+        self.samples = []
         # raw samples: MOE_BENCH_CLOCKS_DIR if set, else the temp directory
         base = os.environ.get("MOE_BENCH_CLOCKS_DIR") or tempfile.gettempdir()
         self.path = os.path.join(base, f"moe_bench_clocks_rank{index}.csv")
 
+    def _nvml_loop(self, stop):
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
+            self.max_mhz = float(pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM))
+            while not stop.is_set():
+                mhz = pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM)
+                bits = pynvml.nvmlDeviceGetCurrentClocksEventReasons(h)
+                self.samples.append((float(mhz), int(bits)))
+                stop.wait(0.02)
+            pynvml.nvmlShutdown()
+        except Exception:  # no NVML: the nvidia-smi record alone
+            return
+
     def start(self):
+        import threading
+        self._stop = threading.Event()
+        self.thread = threading.Thread(target=self._nvml_loop, args=(self._stop,), daemon=True)
+        self.thread.start()
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
@@ -104,9 +131,9 @@ class _Clocks:
         except OSError:
             self.proc = None
 
-    def stop(self):
+    def _smi_rows(self):
         if self.proc is None:
-            return None
+            return []
         time.sleep(0.25)
         self.proc.terminate()
         try:
@@ -123,6 +150,23 @@ class _Clocks:
                 rows.append((float(parts[1]), float(parts[2]), parts[4:]))
             except ValueError:
                 continue
+        return rows
+
+    def stop(self):
+        if self.thread is not None:
+            self._stop.set()
+            self.thread.join(timeout=5)
+        rows = self._smi_rows()
+        if self.samples:
+            mx = getattr(self, "max_mhz", max(m for m, _ in self.samples))
+            reasons = sorted({n for _, b in self.samples for bit, n in self.REASONS.items()
+                              if b & bit})
+            cap = sum(1 for _, b in self.samples if b & 0x4) / len(self.samples)
+            return {"sm_mhz": statistics.median(m for m, _ in self.samples), "sm_max_mhz": mx,
+                    "reasons": reasons, "samples": len(self.samples),
+                    "power_cap_share": cap, "smi_samples": len(rows),
+                    "source": "NVML every 20 ms during the timed region (nvidia-smi every "
+                              "200 ms beside it)"}
         if not rows:
             return None
         mx = max(r[1] for r in rows)
@@ -130,8 +174,10 @@ class _Clocks:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in load for i, v in enumerate(r[2][1:5])
                           if v.lower() == "active"})
+        cap = sum(1 for r in load if r[2][4].lower() == "active") / len(load)
         return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": mx,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "power_cap_share": cap,
+                "source": "nvidia-smi every 200 ms during the timed region"}
 
 
 def _algorithmic(cfg, counts_np, gather=False):
@@ -153,6 +199,34 @@ def _algorithmic(cfg, counts_np, gather=False):
         "rows_ffn": rows_ffn,
     }
     return out
+
+
+def tile_rows(kept, bm=128):
+    """Rows the grouped GEMM computes for segments of `kept` rows: whole
+    128-row tiles, except a last tile holding at most 64 rows, which runs as a
+    64-row half tile."""
+    kept = np.asarray(kept, np.int64)
+    full, rem = kept // bm, kept % bm
+    return int((full * bm + np.where(rem == 0, 0, np.where(rem <= bm // 2, bm // 2, bm))).sum())
+
+
+def layout_metrics(cfg, counts, C):
+    """The layer's load metrics: rows per expert, the drop and padding
+    fractions, and eta = mean over max of the ranks' received rows (the column
+    sums of the count matrix): the useful fraction of the group's expert
+    compute ("Expert parallelism", "Load imbalance becomes idle time")."""
+    counts = np.asarray(counts, np.int64)
+    kept = np.minimum(counts, cfg.capacity) if cfg.capacity else counts
+    loads = np.asarray(C, np.float64).sum(axis=0)
+    rows_kept = int(kept.sum()) + (cfg.T if cfg.has_shared else 0)
+    rows_tiled = tile_rows(kept) + (tile_rows([cfg.T]) if cfg.has_shared else 0)
+    return {"rows_per_expert": {"min": int(counts.min()), "median": float(np.median(counts)),
+                                "max": int(counts.max())},
+            "eta": float(loads.mean() / loads.max()) if loads.max() > 0 else 1.0,
+            "drop_fraction": float(1.0 - kept.sum() / max(cfg.A, 1)),
+            "padding_fraction": float(1.0 - rows_kept / max(rows_tiled, 1)),
+            "rows_kept": rows_kept, "rows_computed": rows_tiled,
+            "capacity_padding_rows": int(cfg.R - kept.sum()) if cfg.capacity else 0}
 
 
 class _L2Flush:
@@ -321,14 +395,25 @@ def _ffn_bytes(cfg, counts_np):
     return w + rows * cfg.d * 2 * 2 + rows * cfg.f * 2 * 2
 
 
-def _roofline(cfg, ffn_ms, ffn_flops, ffn_bytes, pk):
+PEAK_RULE = ("burst bf16 peak, unless sw_power_cap was active in more than half of the clock "
+             "samples of the timed region: then the sustained (power-capped) bf16 peak")
+
+
+def _tensor_peak(pk, clocks):
+    """The bf16 denominator for a kernel timed in this run, by PEAK_RULE."""
+    capped = bool(clocks) and clocks.get("power_cap_share", 0.0) > 0.5
+    if capped and pk["bf16_tflops_sustained"]:
+        return pk["bf16_tflops_sustained"], pk["source"] + " sustained"
+    return pk["bf16_tflops"], pk["source"] + " burst"
+
+
+def _roofline(cfg, ffn_ms, ffn_flops, ffn_bytes, pk, clocks):
     """The dominant kernel (both grouped GEMM launches of a step) against the
-    roofline that bounds it: the measured bf16 peak when its FLOPs take longer
-    than its bytes at the measured copy bandwidth, else HBM.  The kernel runs
-    inside a loop of hundreds of steps under the board power limit, so the
-    sustained bf16 figure is the tensor denominator; the burst fraction is
-    reported beside it."""
-    peak_tf = pk["bf16_tflops_sustained"] or pk["bf16_tflops"]
+    roofline that bounds it: the bf16 peak when its FLOPs take longer than its
+    bytes at the measured copy bandwidth, else HBM.  The bf16 denominator
+    follows PEAK_RULE from this run's own clock samples; both fractions are
+    reported."""
+    peak_tf, src = _tensor_peak(pk, clocks)
     t_flops = ffn_flops / (peak_tf * 1e12)
     t_bytes = ffn_bytes / (pk["hbm_gbs"] * 1e9)
     tflops = ffn_flops / (ffn_ms * 1e-3) / 1e12
@@ -337,10 +422,10 @@ def _roofline(cfg, ffn_ms, ffn_flops, ffn_bytes, pk):
             "algorithmic_flops": ffn_flops}
     if t_flops >= t_bytes:
         base.update({"bound": "tensor", "achieved": tflops, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": tflops / peak_tf,
-                     "peak_source": pk["source"] + (" sustained" if pk["bf16_tflops_sustained"]
-                                                    else " burst"),
-                     "frac_of_burst_peak": tflops / pk["bf16_tflops"]})
+                     "frac": tflops / peak_tf, "peak_source": src, "peak_rule": PEAK_RULE,
+                     "frac_of_burst_peak": tflops / pk["bf16_tflops"],
+                     "frac_of_sustained_peak": (tflops / pk["bf16_tflops_sustained"]
+                                                if pk["bf16_tflops_sustained"] else None)})
     else:
         gbs = ffn_bytes / (ffn_ms * 1e-3) / 1e9
         base.update({"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
@@ -514,14 +599,15 @@ def run_ours(args, cfg):
                                   "L2 flushed between steps"}},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": _roofline(cfg, kt["grouped_ffn"], alg["ffn_flops"], _ffn_bytes(cfg, counts),
-                              pk),
+                              pk, clk),
         "kernels": kernels,
+        "layout": layout_metrics(cfg, counts, layer.count_mat.cpu().numpy()),
         "wall_s": wall,
     }
     if clk:
         res["clocks"] = clk
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(cfg, x, W_r, lbias, layer, budget_s=args.cpu_budget)
+        res["cpu_baseline"] = cpu_baseline(cfg, x, W_r, lbias, layer)
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank == 0:
@@ -539,56 +625,103 @@ def _cores():
     return os.cpu_count()
 
 
-def _oracle_sample(cfg, x_cpu, W_r_cpu, lbias_cpu, experts, n_tokens):
-    """The oracle on the first n_tokens tokens as a complete batch (router,
-    routing, permutation, EP layout, experts, combine).  Returns seconds."""
-    import oracle
-    sub = cfg.with_(T=n_tokens, n_ep=1)
-    xs = x_cpu[:n_tokens]
-    t0 = time.perf_counter()
-    l = oracle.router_logits(xs, W_r_cpu, lbias_cpu)
-    s = (oracle.sigmoid(l) if cfg.score_fn == "sigmoid" else l).astype(np.float32)
-    y, st = oracle.moe_forward(xs, s, sub, *experts)
-    oracle.ep_layout(st["idx"], st["perm"]["inv"], sub.E, 1, sub.T)
-    return time.perf_counter() - t0
+# The oracle's timed sample per workload: (tokens in the sub-batch, routed experts
+# whose rows the expert FFN computes).  Routing, permutation, EP layout and
+# combine run on the whole sub-batch; the expert FFN on the complete segments of
+# a seeded subset of the experts.  Sized so that one sample takes about a
+# second on 16 host cores: a Mixtral expert's 128 rows of the 512-token batch
+# cost 45 GFLOP in fp64, a DeepSeek-V3-shaped expert's 16 rows stream 350 MB of
+# fp64 weights.
+ORACLE_SAMPLE = {"tiny": (1024, 8), "mixtral": (512, 2), "dsv3": (512, 16),
+                 "dsv3_decode": (128, 16), "skew": (4096, 16)}
 
 
-class _HostExperts:
-    def __init__(self, W):
-        self.W, self.c = W, {}
+class OracleSample:
+    """One bounded sample of the workload on the oracle, as it stands: the
+    first n tokens as one complete batch through the oracle's steps in the
+    pages' order (router logits, expert choice and gates, permutation, EP
+    layout, SwiGLU experts, combine), with the expert FFN computed on the rows
+    of a seeded subset S of the routed experts.  The weights of S are upcast to
+    fp64 once, before any timing, so the oracle's own upcast is a no-op and its
+    cost is linear in the rows.  The full step is estimated by scaling the FFN
+    time by (rows of the batch, shared rows included) / (rows of S), then the
+    whole batch by T / n."""
 
-    def __getitem__(self, e):
-        if e not in self.c:
-            self.c[e] = self.W[e].float().cpu().numpy()
-        return self.c[e]
+    def __init__(self, cfg, x, W_r, lbias, expert_weights):
+        """x, W_r, lbias: torch tensors (any device); expert_weights(ids) ->
+        (W1, W3, W2) torch tensors of those experts, [len(ids), ...]."""
+        import oracle
+        self.oracle = oracle
+        n, m = ORACLE_SAMPLE.get(cfg.name, (min(cfg.T, 512), min(cfg.E, 16)))
+        n = min(n, cfg.T)
+        m = min(m, cfg.E)
+        self.cfg = cfg
+        # the sub-batch keeps the workload's capacity factor (rows per expert scale with T)
+        cap = max(1, math.ceil(cfg.capacity * n / cfg.T)) if cfg.capacity else 0
+        self.sub = cfg.with_(T=n, n_ep=math.gcd(n, math.gcd(cfg.n_ep, cfg.E)), capacity=cap)
+        self.x = x[:n].float().cpu().numpy()
+        self.W_r = W_r.cpu().numpy()
+        self.lbias = None if lbias is None else lbias.cpu().numpy()
+        rng = np.random.default_rng(11)
+        self.S = np.sort(rng.choice(cfg.E, m, replace=False))
+        W1, W3, W2 = expert_weights([int(e) for e in self.S])
+        self.W = {}
+        for i, e in enumerate(self.S):
+            self.W[int(e)] = tuple(np.asarray(w[i].float().cpu().numpy(), np.float64)
+                                   for w in (W1, W3, W2))
+        self.n, self.m = n, m
+
+    def run(self):
+        """One sample.  Returns (measured seconds, estimated seconds of the full
+        step, rows of S, rows of the sub-batch)."""
+        o, sub = self.oracle, self.sub
+        W = self.W
+        t0 = time.perf_counter()
+        l = o.router_logits(self.x, self.W_r, self.lbias)
+        s = (o.sigmoid(l) if sub.score_fn == "sigmoid" else l).astype(np.float32)
+        idx = o.select_experts(s, sub.k, None, sub.n_groups, sub.topk_groups)
+        gates = o.gate_weights(s, idx, sub.score_fn, sub.norm_topk)
+        perm = o.permute(idx, sub.E, sub.capacity)
+        o.ep_layout(idx, perm["inv"], sub.E, sub.n_ep, sub.T)
+        t1 = time.perf_counter()
+        segs = [np.arange(int(perm["offsets"][e]), int(perm["offsets"][e] + perm["kept"][e]))
+                for e in W]
+        rows = np.concatenate(segs) if segs else np.zeros(0, np.int64)
+        view = lambda j: {e: W[e][j] for e in W}  # noqa: E731
+        out = o.expert_outputs(self.x, perm, sub.k, view(0), view(1), view(2), rows=rows)
+        t2 = time.perf_counter()
+        o.combine(out, perm, sub.k, gates, sub.T)
+        t3 = time.perf_counter()
+        ffn = t2 - t1
+        rows_all = int(perm["kept"].sum()) + (sub.T if sub.has_shared else 0)
+        est = ((t1 - t0) + (t3 - t2) + ffn * rows_all / max(rows.size, 1)) * self.cfg.T / sub.T
+        return t3 - t0, est, int(rows.size), rows_all
+
+    def describe(self, rows_s, rows_all):
+        return (f"first {self.n} tokens as one batch (router, routing, permutation, EP layout, "
+                f"combine) with the expert FFN on the complete segments of {self.m} seeded "
+                f"experts ({rows_s} of the batch's {rows_all} rows), fp64 weights of those "
+                f"experts upcast once before timing; the full {self.cfg.T}-token step is "
+                f"estimated as (batch time with the FFN scaled by rows) x {self.cfg.T}/{self.n}")
 
 
-def cpu_baseline(cfg, x, W_r, lbias, layer=None, budget_s=15.0, W=None):
-    """Time the oracle, as it stands, on a bounded sample of the workload."""
-    x_cpu = x.float().cpu().numpy()
-    W_r_cpu = W_r.cpu().numpy()
-    lb = None if lbias is None else lbias.cpu().numpy()
-    if W is None:
-        W1 = torch.empty(0)
-        W13 = layer.W13  # packed [n, 2f, d]; unpack the 128-row interleave for the oracle
+def cpu_baseline(cfg, x, W_r, lbias, layer, reps=3):
+    """The oracle, as it stands, on the bounded sample of OracleSample (the
+    same procedure as --impl reference), median of `reps` runs."""
+    def weights(ids):
+        W13, W2 = layer.W13, layer.W2
         n, f2, d = W13.shape
-        f = f2 // 2
-        blk = W13.view(n, f // 128, 2, 128, d)
-        W1 = blk[:, :, 0].reshape(n, f, d)
-        W3 = blk[:, :, 1].reshape(n, f, d)
-        W = (W1, W3, layer.W2)
-    experts = tuple(_HostExperts(w) for w in W)
-    n2 = 8
-    _oracle_sample(cfg, x_cpu, W_r_cpu, lb, experts, n2)  # warms the host copy of the experts
-    t2 = _oracle_sample(cfg, x_cpu, W_r_cpu, lb, experts, n2)
-    # grow the sample until it takes about budget_s seconds (cost is not linear in
-    # the token count for small samples: per-expert weight conversion dominates)
-    while t2 < 0.5 * budget_s and n2 < cfg.T:
-        n2 = int(min(cfg.T, max(2 * n2, n2 * 0.8 * budget_s / max(t2, 1e-6))))
-        t2 = _oracle_sample(cfg, x_cpu, W_r_cpu, lb, experts, n2)
-    return {"value": n2 / t2, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
-            "sample": f"first {n2} tokens of the workload as one batch (router, routing, "
-                      f"permutation, EP layout, SwiGLU experts, combine), fp64 numpy; {t2:.1f} s"}
+        blk = W13[ids].view(len(ids), f2 // 256, 2, 128, d)  # undo the 128-row interleave
+        return (blk[:, :, 0].reshape(len(ids), f2 // 2, d),
+                blk[:, :, 1].reshape(len(ids), f2 // 2, d), W2[ids])
+    samp = OracleSample(cfg, x, W_r, lbias, weights)
+    samp.run()  # warm
+    runs = [samp.run() for _ in range(reps)]
+    meas = statistics.median(r[0] for r in runs)
+    est = statistics.median(r[1] for r in runs)
+    return {"value": cfg.T / est, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+            "sample": samp.describe(runs[0][2], runs[0][3]), "sample_s": meas,
+            "sample_tokens": samp.n, "estimated_step_s": est}
 
 
 def run_reference(args, cfg):
@@ -597,33 +730,28 @@ def run_reference(args, cfg):
         return
     x = synth.make_x(cfg)
     W_r, lbias = synth.make_router(cfg)
-    # weights of every expert (bf16 on the host); the oracle upcasts per expert
-    W1, W3, W2 = synth.make_expert_weights(cfg)
-    experts = tuple(_HostExperts(w) for w in (W1, W3, W2))
-    x_cpu = x.float().numpy()
-    W_r_cpu = W_r.numpy()
-    lb = None if lbias is None else lbias.numpy()
-    budget = max(3.0, min(args.cpu_budget, 150.0 / max(1, args.steps + args.warmup)))
-    n2 = 8
-    _oracle_sample(cfg, x_cpu, W_r_cpu, lb, experts, n2)
-    t = _oracle_sample(cfg, x_cpu, W_r_cpu, lb, experts, n2)
-    while t < 0.5 * budget and n2 < cfg.T:
-        n2 = int(min(cfg.T, max(2 * n2, n2 * 0.8 * budget / max(t, 1e-6))))
-        t = _oracle_sample(cfg, x_cpu, W_r_cpu, lb, experts, n2)
-    for _ in range(max(0, args.warmup - 2)):
-        _oracle_sample(cfg, x_cpu, W_r_cpu, lb, experts, n2)
-    times = [_oracle_sample(cfg, x_cpu, W_r_cpu, lb, experts, n2) for _ in range(args.steps)]
-    sec = float(np.mean(times))
-    v = n2 / sec
+    samp = OracleSample(cfg, x, W_r, lbias,
+                        lambda ids: synth.make_expert_weights(cfg, experts=ids))
+    for _ in range(args.warmup):
+        samp.run()
+    runs = [samp.run() for _ in range(args.steps)]
+    meas = float(np.mean([r[0] for r in runs]))
+    est = float(np.mean([r[1] for r in runs]))
+    v = cfg.T / est
     res = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3 * cfg.T / n2,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": meas * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)",
         "config": {"workload": _workload(cfg), "tokens_per_gpu": cfg.T,
                    "parallelism": "host cores (oracle)"},
+        "timing": {"ms_per_step": "measured time of one sample step (the timed region is "
+                                  "steps x this)",
+                   "estimated_full_step_ms": est * 1e3,
+                   "value": "T / estimated full step"},
         "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
-                         "sample": f"first {n2} tokens per step as one batch, fp64 numpy"},
+                         "sample": samp.describe(runs[0][2], runs[0][3]),
+                         "sample_s": meas, "sample_tokens": samp.n, "estimated_step_s": est},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(res), flush=True)
@@ -634,9 +762,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", default="mixtral", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--config", default="dsv3", choices=sorted(synth.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", default="rows", choices=["rows", "gather"],
                     help="rows: the permute writes x_sorted and GEMM 1 reads it; gather: the "

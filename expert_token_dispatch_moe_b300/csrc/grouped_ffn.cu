@@ -654,16 +654,17 @@ static bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t co
 }
 
 static int set_smem_attr() {
-  static std::once_flag once;
-  static cudaError_t err = cudaSuccess;
-  std::call_once(once, [] {
-    err = cudaFuncSetAttribute(grouped_gemm_kernel<false>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, int(gg::DYN_SMEM));
+  static PerDeviceOnce once;
+  return once.run([] {
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<false>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           int(gg::DYN_SMEM));
     if (err == cudaSuccess)
       err = cudaFuncSetAttribute(grouped_gemm_kernel<true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, int(gg::DYN_SMEM));
+    if (err != cudaSuccess) cudaGetLastError();
+    return err == cudaSuccess ? MOE_OK : MOE_E_CUDA;
   });
-  return err == cudaSuccess ? MOE_OK : MOE_E_CUDA;
 }
 
 #define MOE_TRY_INTERNAL(expr)      \

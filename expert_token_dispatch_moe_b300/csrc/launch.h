@@ -4,6 +4,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "../../include/moe.h"
 #include "common.cuh"
 
@@ -15,6 +18,34 @@ void note_launches(int n);
 
 // Multiprocessors of the current device (cached per device; 148 if unknown).
 int device_sm_count();
+
+// A set-up step whose effect belongs to one device, such as a kernel's opt-in
+// to more than 48 KB of dynamic shared memory (cudaFuncSetAttribute applies to
+// the current device only): run(step) calls step() with the caller's device
+// current the first time that device is seen, and again on a later call if
+// step() failed.  step returns MOE_OK or an error code, which run returns.
+class PerDeviceOnce {
+ public:
+  template <typename F>
+  int run(F&& step) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+      cudaGetLastError();
+      return MOE_E_DEVICE;
+    }
+    if (done_[dev].load(std::memory_order_acquire)) return MOE_OK;
+    std::lock_guard<std::mutex> lk(mu_);
+    if (done_[dev].load(std::memory_order_relaxed)) return MOE_OK;
+    const int rc = step();
+    if (rc == MOE_OK) done_[dev].store(true, std::memory_order_release);
+    return rc;
+  }
+
+ private:
+  static constexpr int kMaxDevices = 64;
+  std::mutex mu_;
+  std::atomic<bool> done_[kMaxDevices] = {};
+};
 
 int launch_router_logits(const moe_cfg& c, const void* x, const float* W, const float* lbias,
                          float* out, int* status, cudaStream_t st);

@@ -507,14 +507,15 @@ int launch_permute(const moe_cfg& c, const void* x, const int32_t* idx, int32_t*
   int32_t* chunk_hist = ws_ptr<int32_t>(ws, L.chunk_hist);
   if (A <= kPermSmallMaxA && c.E <= kPermSmallMaxE) {
     // one CTA does the histogram, the scans and the ranks
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-      attr_err = cudaFuncSetAttribute(perm_index_small_kernel,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      int((64 * (kPermSmallMaxE + 1) + 2 * kPermSmallMaxE) * 4));
+    static PerDeviceOnce once;
+    const int attr_rc = once.run([] {
+      const cudaError_t e = cudaFuncSetAttribute(
+          perm_index_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+          int((64 * (kPermSmallMaxE + 1) + 2 * kPermSmallMaxE) * 4));
+      if (e != cudaSuccess) cudaGetLastError();
+      return e == cudaSuccess ? MOE_OK : MOE_E_CUDA;
     });
-    if (attr_err != cudaSuccess) return MOE_E_CUDA;
+    if (attr_rc != MOE_OK) return attr_rc;
     const size_t smem = size_t(64 * (c.E + 1) + 2 * c.E) * 4;
     perm_index_small_kernel<<<1, kPermSmallThreads, smem, st>>>(
         idx, A, c.E, c.k, c.T / c.n_ep, c.n_ep, c.capacity, src_cnt, counts, offsets, inv, order,

@@ -59,13 +59,17 @@ MOE_API int moe_permute_noalloc(const moe_cfg* c, const moe_bf16* x, const int32
   reset_launches();
   int rc = moe_validate_cfg(c);
   if (rc != MOE_OK) return rc;
-  for (const void* p : {static_cast<const void*>(x), static_cast<const void*>(topk_idx),
-                        static_cast<const void*>(counts), static_cast<const void*>(offsets),
-                        static_cast<const void*>(order), static_cast<const void*>(inv),
-                        static_cast<const void*>(x_sorted)}) {
+  for (const void* p : {static_cast<const void*>(topk_idx), static_cast<const void*>(counts),
+                        static_cast<const void*>(offsets), static_cast<const void*>(order),
+                        static_cast<const void*>(inv)}) {
     if (!p) return MOE_E_NULL;
     if (reinterpret_cast<uintptr_t>(p) & 15u) return MOE_E_ALIGN;
   }
+  // as in moe_permute: x and x_sorted both NULL computes the indices only; one
+  // of them alone is an error
+  for (const void* p : {static_cast<const void*>(x), static_cast<const void*>(x_sorted)})
+    if (reinterpret_cast<uintptr_t>(p) & 15u) return MOE_E_ALIGN;
+  if ((x == nullptr) != (x_sorted == nullptr)) return MOE_E_NULL;
   // The permute touches the status word and histogram counter, the per-(rank,
   // expert) counts and the per-chunk histograms: the workspace regions that
   // precede the EP tables.

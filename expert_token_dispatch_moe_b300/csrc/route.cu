@@ -459,17 +459,18 @@ int launch_router_logits(const moe_cfg& c, const void* x, const float* W, const 
     if (tpb > kRlMaxTok) tpb = kRlMaxTok;
     const int blocks = (c.T + tpb - 1) / tpb;
     const size_t sm = kRlRingBytes + size_t(kRlWarps) * tpb * ep * 4;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
+    static PerDeviceOnce once;
+    const int attr_rc = once.run([] {
       const int mx = int(kRlRingBytes + size_t(kRlWarps) * kRlMaxTok * 16 * 4);
-      attr_err = cudaFuncSetAttribute(router_logits_small_kernel<8>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-      if (attr_err == cudaSuccess)
-        attr_err = cudaFuncSetAttribute(router_logits_small_kernel<16>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+      cudaError_t e = cudaFuncSetAttribute(router_logits_small_kernel<8>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(router_logits_small_kernel<16>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+      if (e != cudaSuccess) cudaGetLastError();
+      return e == cudaSuccess ? MOE_OK : MOE_E_CUDA;
     });
-    if (attr_err != cudaSuccess) return MOE_E_CUDA;
+    if (attr_rc != MOE_OK) return attr_rc;
     if (ep == 8)
       router_logits_small_kernel<8><<<blocks, kRlWarps * 32, sm, st>>>(
           xb, W, lbias, c.T, c.d, c.E, c.score_fn, tpb, status, out);

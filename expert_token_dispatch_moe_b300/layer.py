@@ -86,27 +86,38 @@ class MoELayer:
         `y` (bf16 [T, d] on the device) when given.
 
         With `scores` (fp32 [T, E]) the router step is skipped and the given
-        scores are routed (used to check routing on exact inputs)."""
+        scores are routed (used to check routing on exact inputs).  Each C-ABI
+        call sits in an NVTX range named after it, for profilers' timelines."""
         c = self.cfg
         n = 0
+        push, pop = torch.cuda.nvtx.range_push, torch.cuda.nvtx.range_pop
         if scores is None:
+            push("moe_router_logits")
             moe_router_logits(c, x, self.W_r, self.W_r_split, self.logit_bias, self.scores,
                               self.ws)
+            pop()
             n += moe_last_launch_count()
             scores = self.scores
+        push("moe_route")
         moe_route(c, scores, self.selection_bias, self.topk_idx, self.topk_gate)
+        pop()
         n += moe_last_launch_count()
+        push("moe_permute")
         if self.gather:
             moe_permute(c, None, self.topk_idx, self.counts, self.offsets, self.order, self.inv,
                         None, self.ws)
         else:
             moe_permute(c, x, self.topk_idx, self.counts, self.offsets, self.order, self.inv,
                         self.x_sorted, self.ws)
+        pop()
         n += moe_last_launch_count()
+        push("moe_ep_layout")
         moe_ep_layout(c, self.topk_idx, self.offsets, self.inv, self.count_mat, self.send_off,
                       self.recv_off, self.send_idx, x if self.send_buf is not None else None,
                       self.send_buf, self.ws)
+        pop()
         n += moe_last_launch_count()
+        push("moe_grouped_ffn")
         if self.gather:
             moe_grouped_ffn_gather(c, x, self.order, self.counts, self.offsets, self.W13, self.W2,
                                    self.h, self.y_sorted, self.ws)
@@ -117,9 +128,12 @@ class MoELayer:
         else:
             moe_grouped_ffn(c, self.x_sorted, x if c.has_shared else None, self.counts,
                             self.offsets, self.W13, self.W2, self.h, self.y_sorted, self.ws)
+        pop()
         n += moe_last_launch_count()
         out = self.y if y is None else y
+        push("moe_combine")
         moe_combine(c, self.y_sorted, self.inv, self.topk_gate, out)
+        pop()
         n += moe_last_launch_count()
         self.launches_per_forward = n
         return out

@@ -230,7 +230,11 @@ int moe_dispatch_recv_fp8(const moe_cfg* cfg, const uint8_t* send_fp8, const flo
  *    different streams, or from host threads without ordering) race on it.
  *  - Each call clears the status word and counters it uses.  Bad expert ids are
  *    treated as dropped (inv = -1) as in moe_permute, but the status word is not
- *    readable from outside.
+ *    readable from outside: such ids are dropped silently.
+ *  - The per-(source rank, expert) histogram stays in the hidden array, so
+ *    moe_ep_layout and moe_ep_layout_fp8, which read it from the workspace of
+ *    the preceding moe_permute, cannot follow this call; run moe_permute with a
+ *    workspace when the layout is needed.
  *  - The call allocates and frees nothing. */
 int moe_permute_noalloc(const moe_cfg* cfg, const moe_bf16* x, const int32_t* topk_idx,
                         int32_t* counts, int32_t* offsets, int32_t* order, int32_t* inv,

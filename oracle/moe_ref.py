@@ -16,8 +16,8 @@ import numpy as np
 
 __all__ = [
     "router_logits", "sigmoid", "select_experts", "gate_weights",
-    "capacity_rows", "permute", "ep_layout", "swiglu_expert",
-    "expert_outputs", "combine", "moe_forward", "dense_mask_forward",
+    "capacity_rows", "permute", "ep_layout", "swiglu_hidden", "swiglu_expert",
+    "expert_outputs", "expert_rows", "combine", "moe_forward", "dense_mask_forward",
     "imbalance_eta", "alltoall_bytes", "dispatch_combine_bytes_per_token",
     "bias_update", "eplb_replicate", "eplb_pack", "eplb_plan", "eplb_dispatch",
     "E4M3_MAX", "e4m3_encode", "e4m3_decode", "quantize_rows_fp8", "dequantize_rows_fp8",
@@ -231,16 +231,23 @@ def ep_layout(idx, inv, E, n_ep, T):
 # Step 5: expert compute ([EP] step 5; "How many bytes move": SwiGLU expert)
 # ----------------------------------------------------------------------------
 
-def swiglu_expert(X, W1, W3, W2):
-    """SwiGLU expert on rows X (fp64): W2 (silu(W1 x) * (W3 x)), with
-    silu(u) = u / (1 + exp(-u)).  W1, W3: [f, d]; W2: [d, f] (out, in).  One
-    expert holds the three d-by-d_e matrices of [EP] "DeepSeek-V3's layout,
-    counted" and costs 6*d*d_e FLOPs per row ([EP] "A worked example")."""
+def swiglu_hidden(X, W1, W3):
+    """The SwiGLU expert's hidden activations on rows X (fp64): h = silu(W1 x) *
+    (W3 x), with silu(u) = u / (1 + exp(-u)).  W1, W3: [f, d] (out, in).  This is
+    the first two of the expert's three d-by-d_e products ([EP] "DeepSeek-V3's
+    layout, counted"); the grouped FFN keeps h between its two products."""
     X = np.asarray(X, F64)
     u = X @ np.asarray(W1, F64).T
     v = X @ np.asarray(W3, F64).T
-    h = (u / (1.0 + np.exp(-u))) * v
-    return h @ np.asarray(W2, F64).T
+    return (u / (1.0 + np.exp(-u))) * v
+
+
+def swiglu_expert(X, W1, W3, W2):
+    """SwiGLU expert on rows X (fp64): W2 (silu(W1 x) * (W3 x)).  W2: [d, f]
+    (out, in).  One expert holds the three d-by-d_e matrices of [EP]
+    "DeepSeek-V3's layout, counted" and costs 6*d*d_e FLOPs per row ([EP] "A
+    worked example")."""
+    return swiglu_hidden(X, W1, W3) @ np.asarray(W2, F64).T
 
 
 def expert_outputs(x, perm, k, W1, W3, W2, rows=None):
@@ -261,6 +268,28 @@ def expert_outputs(x, perm, k, W1, W3, W2, rows=None):
         if rr.size:
             out[rr] = swiglu_expert(x[order[rr] // k], W1[e], W3[e], W2[e])
     return out
+
+
+def expert_rows(x, perm, k, W1, W3, W2, rows):
+    """Hidden activations and outputs of chosen rows of the expert-grouped
+    buffer (step 5, each expert on its contiguous segment), computed expert by
+    expert.  rows: row ids in [0, R); a row past its expert's kept rows (capacity
+    padding) gives zeros.  Returns (h fp64 [n, f], out fp64 [n, d]) in the order
+    of `rows`."""
+    rows = np.asarray(rows, np.int64)
+    order, offsets, kept = perm["order"], perm["offsets"], perm["kept"]
+    x = np.asarray(x)
+    f = np.asarray(W1[0]).shape[0]
+    h = np.zeros((rows.size, f), F64)
+    out = np.zeros((rows.size, x.shape[1]), F64)
+    for e in range(kept.size):
+        lo, hi = int(offsets[e]), int(offsets[e]) + int(kept[e])
+        sel = np.nonzero((rows >= lo) & (rows < hi))[0]
+        if sel.size:
+            X = x[order[rows[sel]] // k]
+            h[sel] = swiglu_hidden(X, W1[e], W3[e])
+            out[sel] = h[sel] @ np.asarray(W2[e], F64).T
+    return h, out
 
 
 def combine(out_rows, perm, k, gates, T, shared_out=None):

@@ -10,7 +10,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 def test_reference_arm_prints_one_contract_line():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                          "--config", "tiny", "--steps", "1", "--warmup", "0", "--cpu-budget", "2"],
+                          "--config", "tiny", "--steps", "2", "--warmup", "0"],
                          capture_output=True, text=True, timeout=600, cwd=ROOT)
     assert out.returncode == 0, out.stderr[-2000:]
     lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
@@ -23,3 +23,29 @@ def test_reference_arm_prints_one_contract_line():
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
     assert d["config"]["workload"].startswith("tiny")
+    # ms_per_step is the measured sample step, so steps x ms_per_step is the timed region
+    assert abs(d["ms_per_step"] - 1e3 * d["cpu_baseline"]["sample_s"]) < 1e-6
+    assert d["timing"]["estimated_full_step_ms"] > 0
+
+
+def test_layout_metrics_eta_matches_the_oracle():
+    """bench.py's eta (mean over max of the count matrix's column sums) is the
+    oracle's imbalance_eta, and its padding fraction follows the tile rule."""
+    import importlib.util
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import oracle
+    import synth
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    rng = np.random.default_rng(3)
+    for n_ep in (2, 8, 64):
+        C = rng.integers(0, 50, size=(n_ep, n_ep))
+        C[0, 0] += 1
+        cfg = synth.CONFIGS["tiny"].with_(n_ep=n_ep, E=64)
+        counts = rng.integers(0, 300, size=64)
+        got = b.layout_metrics(cfg, counts, C)
+        assert got["eta"] == oracle.imbalance_eta(C)
+    # tiles: 300 rows -> 128 + 128 + a 64-row half tile; 200 -> 128 + 128; 0 -> nothing
+    assert b.tile_rows([300, 200, 0, 64, 65]) == 320 + 256 + 0 + 64 + 128

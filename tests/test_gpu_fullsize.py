@@ -1,9 +1,10 @@
 """Parity at the full workload sizes, in the launch configuration the
 benchmark times (the whole MoELayer path on one stream).  Routing, counts,
-offsets and permutations are compared in full elsewhere (test_gpu_parity.py
-runs them at these sizes); here the layer output is compared on a seeded
-sample of tokens that the oracle computes one by one in fp64, and the router
-logits on the same sample."""
+offsets, permutations and the EP layout are compared in full, bit for bit.
+The grouped FFN is compared on rows drawn from every tile it computes: each
+(expert, 128-row block) and each segment's last row, its hidden activations h
+and outputs y_sorted against the fp64 expert; the layer output on tokens that
+own those rows; the router logits on a seeded token sample."""
 import numpy as np
 import pytest
 import torch
@@ -35,9 +36,30 @@ def m():
     return mod
 
 
-@pytest.mark.parametrize("name,n_sample", [("mixtral", 24), ("dsv3", 10), ("dsv3_decode", 8),
-                                           ("skew", 48)])
-def test_full_size_layer_on_sampled_tokens(m, name, n_sample):
+def stratified_rows(perm, seed, block=128):
+    """Rows of the expert-grouped buffer that cover every tile: one seeded
+    random kept row from every (expert, 128-row block) of each segment, and
+    each segment's last kept row (where ragged tails and half tiles sit)."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    for e in range(perm["kept"].size):
+        lo, kept = int(perm["offsets"][e]), int(perm["kept"][e])
+        for b in range(0, kept, block):
+            rows.append(lo + int(rng.integers(b, min(kept, b + block))))
+        if kept:
+            rows.append(lo + kept - 1)
+    return np.unique(np.array(rows, np.int64))
+
+
+# Rows compared per workload (each expert's segment, every 128-row block):
+#   mixtral      8 experts x 8-9 blocks + last rows          ~ 80 rows
+#   dsv3         256 experts x 2-3 blocks + last rows        ~ 800 rows (+ 3 shared)
+#   dsv3_decode  ~250 non-empty experts x (1 block + last)   ~ 480 rows (+ 3 shared)
+#   skew         64 experts x 3-5 blocks (capacity 640)      ~ 230 rows
+# The layer output y is compared on up to 48 tokens that own compared rows (the
+# first and last token included).
+@pytest.mark.parametrize("name", ["mixtral", "dsv3", "dsv3_decode", "skew"])
+def test_full_size_every_tile_against_oracle(m, name):
     cfg = synth.CONFIGS[name]
     dev = torch.device("cuda")
     x = synth.make_x(cfg, device=dev)
@@ -47,19 +69,42 @@ def test_full_size_layer_on_sampled_tokens(m, name, n_sample):
     layer.forward(x, scores=scores)
     torch.cuda.synchronize()
     assert m.moe_get_device_status(layer.ws) == 0
-    tokens = synth.sample_tokens(cfg, n_sample).numpy()
     s_np = scores.cpu().numpy()
     x_np = x.float().cpu().numpy()
-    y_ref, st = oracle.moe_forward(x_np, s_np, cfg, StreamedExperts(W1), StreamedExperts(W3),
-                                   StreamedExperts(W2), tokens=tokens)
     # routing and permutation in full, bit-exact
-    assert np.array_equal(npi(layer.topk_idx), st["idx"])
-    assert np.array_equal(npi(layer.counts), st["perm"]["counts"])
-    assert np.array_equal(npi(layer.inv), st["perm"]["inv"])
-    lay = oracle.ep_layout(st["idx"], st["perm"]["inv"], cfg.E, cfg.n_ep, cfg.T)
+    idx = oracle.select_experts(s_np, cfg.k, None, cfg.n_groups, cfg.topk_groups)
+    perm = oracle.permute(idx, cfg.E, cfg.capacity)
+    assert np.array_equal(npi(layer.topk_idx), idx)
+    assert np.array_equal(npi(layer.counts), perm["counts"])
+    assert np.array_equal(npi(layer.offsets), perm["offsets"])
+    assert np.array_equal(npi(layer.inv), perm["inv"])
+    lay = oracle.ep_layout(idx, perm["inv"], cfg.E, cfg.n_ep, cfg.T)
     assert np.array_equal(npi(layer.count_mat), lay["C"])
     assert np.array_equal(npi(layer.send_idx), lay["send_idx"])
-    # layer output on the sampled tokens
+
+    # every tile's rows: h and y_sorted against the fp64 expert
+    rows = stratified_rows(perm, seed=5)
+    h_ref, out_ref = oracle.expert_rows(x_np, perm, cfg.k, StreamedExperts(W1),
+                                        StreamedExperts(W3), StreamedExperts(W2), rows)
+    ridx = torch.from_numpy(rows).to(dev)
+    assert_y_close(npf(layer.h[ridx]), h_ref)
+    assert_y_close(npf(layer.y_sorted[ridx]), out_ref)
+    if cfg.has_shared:
+        tt = np.array([0, cfg.T // 2 + 1, cfg.T - 1])
+        E = cfg.E
+        sidx = torch.from_numpy(cfg.R + tt).to(dev)
+        assert_y_close(npf(layer.h[sidx]),
+                       oracle.swiglu_hidden(x_np[tt], npf(W1[E]), npf(W3[E])))
+        assert_y_close(npf(layer.y_sorted[sidx]),
+                       oracle.swiglu_expert(x_np[tt], npf(W1[E]), npf(W3[E]), npf(W2[E])))
+
+    # the layer output on tokens that own compared rows
+    owners = np.unique(perm["order"][rows] // cfg.k)
+    rng = np.random.default_rng(6)
+    tokens = np.unique(np.concatenate([rng.choice(owners, min(46, owners.size), replace=False),
+                                       [0, cfg.T - 1]]))
+    y_ref, _ = oracle.moe_forward(x_np, s_np, cfg, StreamedExperts(W1), StreamedExperts(W3),
+                                  StreamedExperts(W2), tokens=tokens)
     assert_y_close(npf(layer.y[torch.from_numpy(tokens).to(dev)]), y_ref[tokens])
 
 

@@ -271,6 +271,47 @@ def test_single_expert_is_a_swiglu_mlp():
     assert np.allclose(y, ref.numpy(), rtol=1e-12, atol=1e-12)
 
 
+def test_swiglu_hidden_against_torch_fp64():
+    """h = silu(W1 x) * (W3 x), with torch.nn.functional's silu in fp64 as the
+    independent reference, on several experts' weights."""
+    cfg = _tiny(E=3, T=10, d=32, f=16)
+    x, s, W1, W3, W2 = _inputs(cfg, seed=4)
+    xt = torch.from_numpy(x).double()
+    for e in range(cfg.E):
+        ref = (F.silu(F.linear(xt, torch.from_numpy(W1[e]).double())) *
+               F.linear(xt, torch.from_numpy(W3[e]).double()))
+        assert np.allclose(oracle.swiglu_hidden(x, W1[e], W3[e]), ref.numpy(), rtol=1e-13,
+                           atol=1e-14)
+
+
+@pytest.mark.parametrize("kw", [dict(E=6, k=2), dict(E=4, k=2, capacity=4),
+                                dict(E=8, k=3, score_fn="sigmoid", norm_topk=1, n_groups=4,
+                                     topk_groups=2)])
+def test_expert_rows_per_row_brute_force(kw):
+    """Each requested row of the grouped buffer: its token and expert looked up
+    row by row, h and the output recomputed with torch.nn.functional in fp64;
+    capacity padding rows are zero."""
+    cfg = _tiny(T=16, **kw)
+    x, s, W1, W3, W2 = _inputs(cfg, seed=5)
+    idx = oracle.select_experts(s, cfg.k, None, cfg.n_groups, cfg.topk_groups)
+    perm = oracle.permute(idx, cfg.E, cfg.capacity)
+    R = perm["order"].size
+    rows = np.array(sorted(set([0, R - 1] + list(range(1, R, 3)))))
+    h, out = oracle.expert_rows(x, perm, cfg.k, W1, W3, W2, rows)
+    xt = torch.from_numpy(x).double()
+    for n, r in enumerate(rows):
+        a = perm["order"][r]
+        if a < 0:
+            assert not h[n].any() and not out[n].any()
+            continue
+        t, e = a // cfg.k, idx.reshape(-1)[a]
+        hr = (F.silu(F.linear(xt[t], torch.from_numpy(W1[e]).double())) *
+              F.linear(xt[t], torch.from_numpy(W3[e]).double()))
+        orr = F.linear(hr, torch.from_numpy(W2[e]).double())
+        assert np.allclose(h[n], hr.numpy(), rtol=1e-12, atol=1e-14)
+        assert np.allclose(out[n], orr.numpy(), rtol=1e-12, atol=1e-14)
+
+
 @pytest.mark.parametrize("kw", [
     dict(),
     dict(E=8, k=3, score_fn="sigmoid", norm_topk=1, n_groups=4, topk_groups=2, has_shared=1),
@@ -466,3 +507,16 @@ def test_planted_group_score_top1_only_is_caught(monkeypatch):
         return r
     monkeypatch.setattr(moe_ref, "np", _NumpyMutant(sort=sort_zero_second))
     assert _fails(lambda: test_select_matches_brute_force(12, 4, 3, 2))
+
+
+def test_planted_wrong_expert_in_expert_rows_is_caught(monkeypatch):
+    """expert_rows taking the next expert's weights for a segment fails its
+    row-by-row brute force."""
+    real = moe_ref.swiglu_hidden
+    calls = {"n": 0}
+
+    def shifted(X, W1, W3):
+        calls["n"] += 1
+        return real(X, W3, W1) if calls["n"] % 2 == 0 else real(X, W1, W3)
+    monkeypatch.setattr(moe_ref, "swiglu_hidden", shifted)
+    assert _fails(lambda: test_expert_rows_per_row_brute_force(dict(E=6, k=2)))

@@ -73,3 +73,26 @@ def test_noalloc_rejects_configurations_beyond_its_scratch(m):
         m.moe_permute_noalloc(c, x, idx, out["counts"], out["offsets"], out["order"],
                               out["inv"], out["x_sorted"])
     assert ei.value.code == -9
+
+
+def test_noalloc_indices_only_mode(m):
+    """x and x_sorted both NULL: the indices alone, equal to moe_permute's in the
+    same mode; one of the two alone is rejected as in moe_permute."""
+    cfg = CASES["dsv3"]
+    c = m.MoeCfg.from_layer(cfg)
+    ws = torch.zeros(m.moe_workspace_bytes(c), dtype=torch.uint8, device="cuda")
+    m.moe_workspace_init(c, ws)
+    for seed in (2, 3):
+        _, idx = _inputs(cfg, seed)
+        ref, got = _outputs(cfg), _outputs(cfg)
+        m.moe_permute(c, None, idx, ref["counts"], ref["offsets"], ref["order"], ref["inv"],
+                      None, ws)
+        m.moe_permute_noalloc(c, None, idx, got["counts"], got["offsets"], got["order"],
+                              got["inv"], None)
+        torch.cuda.synchronize()
+        for key in ("counts", "offsets", "order", "inv"):
+            assert torch.equal(got[key], ref[key]), (seed, key)
+    with pytest.raises(m.MoeError) as ei:
+        m.moe_permute_noalloc(c, None, idx, got["counts"], got["offsets"], got["order"],
+                              got["inv"], got["x_sorted"])
+    assert ei.value.code == -1
