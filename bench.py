@@ -103,18 +103,28 @@ class _Clocks:
         self.path = os.path.join(base, f"moe_bench_clocks_rank{index}.csv")
 
     def _nvml_loop(self, stop):
+        """Read-only NVML queries through the driver's libnvidia-ml (ctypes)."""
+        import ctypes
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
-            self.max_mhz = float(pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM))
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit_v2 failed")
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+                raise RuntimeError("nvmlDeviceGetHandleByIndex_v2 failed")
+            reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            mhz, mx, bits = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+            if nv.nvmlDeviceGetMaxClockInfo(h, ctypes.c_int(1), ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
             while not stop.is_set():
-                mhz = pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM)
-                bits = pynvml.nvmlDeviceGetCurrentClocksEventReasons(h)
-                self.samples.append((float(mhz), int(bits)))
+                if (nv.nvmlDeviceGetClockInfo(h, ctypes.c_int(1), ctypes.byref(mhz)) == 0 and
+                        reasons_fn(h, ctypes.byref(bits)) == 0):
+                    self.samples.append((float(mhz.value), int(bits.value)))
                 stop.wait(0.02)
-            pynvml.nvmlShutdown()
-        except Exception:  # no NVML: the nvidia-smi record alone
+            nv.nvmlShutdown()
+        except Exception as exc:  # no NVML: the nvidia-smi record alone
+            self.nvml_error = f"{type(exc).__name__}: {exc}"
             return
 
     def start(self):
@@ -170,6 +180,7 @@ class _Clocks:
         if not rows:
             return None
         mx = max(r[1] for r in rows)
+        extra = {"nvml_error": self.nvml_error} if getattr(self, "nvml_error", None) else {}
         load = [r for r in rows if r[0] > 0.3 * mx] or rows
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in load for i, v in enumerate(r[2][1:5])
@@ -177,7 +188,7 @@ class _Clocks:
         cap = sum(1 for r in load if r[2][4].lower() == "active") / len(load)
         return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": mx,
                 "reasons": reasons, "samples": len(rows), "power_cap_share": cap,
-                "source": "nvidia-smi every 200 ms during the timed region"}
+                "source": "nvidia-smi every 200 ms during the timed region", **extra}
 
 
 def _algorithmic(cfg, counts_np, gather=False):
@@ -514,36 +525,37 @@ def run_ours(args, cfg):
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed steps")
 
-    # end to end through the public API, host buffers (pinned) in and out
+    # end to end through the library's host call (moe_layer_forward_host): pinned
+    # host x in and y out, one copy per direction per batch on copy streams, the
+    # forward issued from C.  Serial: one batch per call, L2 flushed between
+    # steps, so each step's copies and compute run back to back.
     x_host = x.cpu().pin_memory()
     y_host = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
-    x_dev = torch.empty_like(x)
     e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
              for _ in range(args.steps)]
     for _ in range(2):
-        layer.forward_host(x_host, y_host, x_dev)
+        layer.forward_host_c([x_host], [y_host])
     torch.cuda.synchronize(dev)
     for i in range(args.steps):
         flush()
         e_evs[i][0].record(st)
-        layer.forward_host(x_host, y_host, x_dev)
+        layer.forward_host_c([x_host], [y_host])
         e_evs[i][1].record(st)
     torch.cuda.synchronize(dev)
     e2e_serial_ms = float(np.mean([a.elapsed_time(b) for a, b in e_evs]))
 
-    # the same through the streaming call: each step's host->device copy and the
-    # previous step's device->host copy overlap compute (copy streams); the
-    # whole run of `steps` batches is timed, so every step's copies are inside
-    # the region.  No flush between steps here: the weights a step streams
-    # (>= 1 GB on the large workloads) are far larger than L2.
+    # streamed: all `steps` batches in one call, each batch's host->device copy
+    # and the previous batch's device->host copy overlapping compute; the whole
+    # run is timed, so every step's copies are inside the region.  No flush
+    # between steps here: the weights a step streams (>= 1 GB on the large
+    # workloads) are far larger than L2.
     x_hosts, y_hosts = [x_host] * args.steps, [y_host] * args.steps
-    layer.capture_graphs()   # one graph replay per batch instead of ~10 calls
-    layer.forward_host_stream(x_hosts[:3], y_hosts[:3])
+    layer.forward_host_c(x_hosts[:3], y_hosts[:3])
     torch.cuda.synchronize(dev)
     flush()
     s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s_ev.record(st)
-    layer.forward_host_stream(x_hosts, y_hosts)
+    layer.forward_host_c(x_hosts, y_hosts)
     e_ev.record(st)
     torch.cuda.synchronize(dev)
     e2e_ms = s_ev.elapsed_time(e_ev) / args.steps
@@ -590,13 +602,13 @@ def run_ours(args, cfg):
         "e2e": {"value": cfg.T * world / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 2,
                 "ms_per_step": e2e_ms,
-                "how": "MoELayer.forward_host_stream over all steps (pinned host x in, y out; "
-                       "copies on their own streams overlapping compute; the forward "
-                       "replayed from CUDA graphs)",
+                "how": "moe_layer_forward_host (C ABI) over all steps: pinned host x in, y "
+                       "out, one cudaMemcpyAsync per direction per batch on copy streams "
+                       "overlapping compute, two device buffers per side",
                 "serial": {"value": cfg.T * world / (e2e_serial_ms * 1e-3),
                            "ms_per_step": e2e_serial_ms,
-                           "how": "MoELayer.forward_host per step (copy in, layer, copy out), "
-                                  "L2 flushed between steps"}},
+                           "how": "moe_layer_forward_host with one batch per call (copy in, "
+                                  "layer, copy out), L2 flushed between steps"}},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": _roofline(cfg, kt["grouped_ffn"], alg["ffn_flops"], _ffn_bytes(cfg, counts),
                               pk, clk),

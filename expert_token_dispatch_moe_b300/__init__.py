@@ -35,7 +35,7 @@ EXPORTS = ("moe_validate_cfg", "moe_grouped_rows", "moe_workspace_bytes", "moe_w
            "moe_eplb_dispatch", "moe_pack_backward", "moe_combine_backward",
            "moe_backward_workspace_bytes", "moe_grouped_ffn_backward", "moe_permute_backward",
            "moe_selftest_wait_timeout", "moe_get_device_status", "moe_strerror",
-           "moe_last_launch_count")
+           "moe_last_launch_count", "moe_layer_forward", "moe_layer_forward_host")
 
 
 class MoeError(RuntimeError):
@@ -72,6 +72,27 @@ class MoeCfg(ctypes.Structure):
 
 _P = ctypes.c_void_p
 _CFG = ctypes.POINTER(MoeCfg)
+
+
+class MoeLayerBufs(ctypes.Structure):
+    """struct moe_layer: the layer's weights and step buffers (device pointers)."""
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("W_r", "W_r_split", "logit_bias", "selection_bias", "W13", "W2", "scores",
+                 "topk_idx", "topk_gate", "counts", "offsets", "order", "inv", "x_sorted",
+                 "count_mat", "send_off", "recv_off", "send_idx", "send_buf", "h", "y_sorted",
+                 "ws")] + [("ws_bytes", ctypes.c_size_t)]
+
+    @classmethod
+    def of(cls, **tensors) -> "MoeLayerBufs":
+        b = cls()
+        for name, _ in cls._fields_[:-1]:
+            setattr(b, name, _ptr(tensors.get(name)))
+        ws = tensors.get("ws")
+        b.ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+        return b
+
+
+_LAYER = ctypes.POINTER(MoeLayerBufs)
 _SZ = ctypes.c_size_t
 _sig = {
     "moe_validate_cfg": (ctypes.c_int, [_CFG]),
@@ -107,6 +128,11 @@ _sig = {
     "moe_get_device_status": (ctypes.c_int, [_P, _P]),
     "moe_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_last_launch_count": (ctypes.c_int, []),
+    "moe_layer_forward": (ctypes.c_int, [_CFG, _LAYER, _P, _P, _P]),
+    "moe_layer_forward_host": (ctypes.c_int, [_CFG, _LAYER, ctypes.c_int,
+                                              ctypes.POINTER(_P), ctypes.POINTER(_P),
+                                              ctypes.POINTER(_P), ctypes.POINTER(_P),
+                                              _P, _P, _P]),
 }
 for _name, (_res, _args) in _sig.items():
     _fn = getattr(_lib, _name)
@@ -314,6 +340,31 @@ def moe_strerror(code) -> str:
 
 def moe_last_launch_count() -> int:
     return _lib.moe_last_launch_count()
+
+
+
+
+def moe_layer_forward(cfg, bufs, x, y, stream=None):
+    """bufs: MoeLayerBufs.  The whole forward on device tokens x into y."""
+    _check(_lib.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(bufs), _ptr(x), _ptr(y),
+                                  _stream(stream)), "moe_layer_forward")
+
+
+def moe_layer_forward_host(cfg, bufs, x_hosts, y_hosts, x_devs, y_devs, compute_stream=None,
+                           copy_in_stream=None, copy_out_stream=None):
+    """The forward over pinned host batches x_hosts -> y_hosts (equal-length
+    lists of bf16 [T, d] page-locked CPU tensors), with two device buffers per
+    side; returns once enqueued (the compute stream completes after the last
+    copy out)."""
+    n = len(x_hosts)
+    if len(y_hosts) != n or len(x_devs) != 2 or len(y_devs) != 2:
+        raise ValueError("x_hosts and y_hosts of equal length, two device buffers per side")
+    arr = lambda ts: (_P * max(len(ts), 1))(*[_ptr(t) for t in ts])  # noqa: E731
+    _check(_lib.moe_layer_forward_host(
+        ctypes.byref(cfg), ctypes.byref(bufs), n, arr(x_hosts), arr(y_hosts), arr(x_devs),
+        arr(y_devs), _stream(compute_stream), _stream(copy_in_stream),
+        None if copy_out_stream is None else _stream(copy_out_stream)),
+        "moe_layer_forward_host")
 
 
 from .layer import MoELayer  # noqa: E402,F401

@@ -25,6 +25,9 @@
 // tensor memory and returns.
 #include <cudaTypedefs.h>
 
+#include <stdlib.h>
+#include <string.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -641,8 +644,9 @@ static bool get_encoder() {
 
 // 2-D bf16 row-major [rows, cols] tensor, box = 64 columns x box_rows rows,
 // 128-byte swizzle, out-of-bounds elements read as zero.
-static bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
-                     uint32_t box_rows) {
+bool make_bf16_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
+                   uint32_t box_rows) {
+  if (!get_encoder()) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
   cuuint32_t box[2] = {64, box_rows};
@@ -732,9 +736,9 @@ int launch_router_tc(const moe_cfg& c, const void* x, const void* W_split, const
   // MMA width: the experts rounded up to 16 (at most 256 per tile)
   const int nm = c.E >= BN ? BN : ((c.E + 15) & ~15);
   CUtensorMap mA, mA64, mB;
-  if (!make_map(&mA, x, uint64_t(c.T), c.d, BM)) return MOE_E_CUDA;
-  if (!make_map(&mA64, x, uint64_t(c.T), c.d, BM / 2)) return MOE_E_CUDA;
-  if (!make_map(&mB, W_split, uint64_t(3) * c.E, c.d, uint32_t(nm))) return MOE_E_CUDA;
+  if (!make_bf16_map(&mA, x, uint64_t(c.T), c.d, BM)) return MOE_E_CUDA;
+  if (!make_bf16_map(&mA64, x, uint64_t(c.T), c.d, BM / 2)) return MOE_E_CUDA;
+  if (!make_bf16_map(&mB, W_split, uint64_t(3) * c.E, c.d, uint32_t(nm))) return MOE_E_CUDA;
   const int sms = sm_count();
   if (sms <= 0) return MOE_E_CUDA;
   GroupedParams p{};
@@ -809,14 +813,37 @@ int launch_pack_router(const moe_cfg& c, const float* W, void* out, cudaStream_t
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_E_CUDA;
 }
 
+// Which tiles run the forward FFN.  The pair tiles (grouped_pair.cu) stage a
+// third fewer bytes per MMA but stream a weight block once per 256-token
+// block; the one-SM 128-row tiles of this file keep more weight bytes in
+// flight.  Measured on B300, the pair tiles win when an expert holds about a
+// thousand rows (Mixtral-shaped layer, FFN 1.94 against 1.99 ms) and lose at
+// 256 rows per expert (DeepSeek-V3-shaped layer, 6.59 against 6.31 ms), at
+// the skewed layer's capacity of 640 and at decode sizes.  So the pair tiles
+// take layers whose expected rows per expert, T*k/E (at most the capacity),
+// reach 768.  The environment variable MOE_FFN_TILES = "pair" or "single"
+// overrides the choice (read at every call).  The gathered and training forms
+// always take the one-SM tiles.
+static bool use_pair_tiles(const moe_cfg& c) {
+  const char* v = getenv("MOE_FFN_TILES");
+  if (v && strcmp(v, "pair") == 0) return true;
+  if (v && strcmp(v, "single") == 0) return false;
+  long long rows = (long long)c.T * c.k / c.E;
+  if (c.capacity && rows > c.capacity) rows = c.capacity;
+  return rows >= 768;
+}
+
 int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
                        const int32_t* gather_order, const int32_t* counts, const int32_t* offsets,
                        const void* W13, const void* W2, void* h, void* y_sorted, void* g1,
                        void* ws, cudaStream_t st) {
   using namespace gg;
   if (!get_encoder()) return MOE_E_CUDA;
-  if (set_smem_attr() != MOE_OK) return MOE_E_CUDA;
   const WsLayout L = ws_layout(c);
+  if (gather_order == nullptr && g1 == nullptr && use_pair_tiles(c))
+    return launch_grouped_ffn_pair(c, x_sorted, x, counts, offsets, W13, W2, h, y_sorted,
+                                   ws_ptr<int>(ws, L.status), st);
+  if (set_smem_attr() != MOE_OK) return MOE_E_CUDA;
   const int R = c.capacity ? c.E * c.capacity : c.T * c.k;
   const int n_exp = c.E + c.has_shared;
   const uint64_t rows_h = uint64_t(R) + (c.has_shared ? c.T : 0);
@@ -828,18 +855,18 @@ int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
   const uint64_t a1s_rows = a1s_x ? uint64_t(c.T) : uint64_t(R);
   if (gather_order) {
     // routed rows gathered from the token rows: a map whose box is one row high
-    if (!make_map(&mA1, x, uint64_t(c.T), c.d, 1)) return MOE_E_CUDA;
+    if (!make_bf16_map(&mA1, x, uint64_t(c.T), c.d, 1)) return MOE_E_CUDA;
     mA1h = mA1;
   } else {
-    if (!make_map(&mA1, x_sorted, uint64_t(R), c.d, BM)) return MOE_E_CUDA;
-    if (!make_map(&mA1h, x_sorted, uint64_t(R), c.d, BM / 2)) return MOE_E_CUDA;
+    if (!make_bf16_map(&mA1, x_sorted, uint64_t(R), c.d, BM)) return MOE_E_CUDA;
+    if (!make_bf16_map(&mA1h, x_sorted, uint64_t(R), c.d, BM / 2)) return MOE_E_CUDA;
   }
-  if (!make_map(&mA1s, a1s, a1s_rows, c.d, BM)) return MOE_E_CUDA;
-  if (!make_map(&mA1sh, a1s, a1s_rows, c.d, BM / 2)) return MOE_E_CUDA;
-  if (!make_map(&mB1, W13, uint64_t(n_exp) * 2 * c.f, c.d, BN)) return MOE_E_CUDA;
-  if (!make_map(&mA2, h, rows_h, c.f, BM)) return MOE_E_CUDA;
-  if (!make_map(&mA2h, h, rows_h, c.f, BM / 2)) return MOE_E_CUDA;
-  if (!make_map(&mB2, W2, uint64_t(n_exp) * c.d, c.f, BN)) return MOE_E_CUDA;
+  if (!make_bf16_map(&mA1s, a1s, a1s_rows, c.d, BM)) return MOE_E_CUDA;
+  if (!make_bf16_map(&mA1sh, a1s, a1s_rows, c.d, BM / 2)) return MOE_E_CUDA;
+  if (!make_bf16_map(&mB1, W13, uint64_t(n_exp) * 2 * c.f, c.d, BN)) return MOE_E_CUDA;
+  if (!make_bf16_map(&mA2, h, rows_h, c.f, BM)) return MOE_E_CUDA;
+  if (!make_bf16_map(&mA2h, h, rows_h, c.f, BM / 2)) return MOE_E_CUDA;
+  if (!make_bf16_map(&mB2, W2, uint64_t(n_exp) * c.d, c.f, BN)) return MOE_E_CUDA;
 
   // grid: at most one CTA per SM, no more than an upper bound on the tiles
   const int sms = sm_count();
@@ -884,7 +911,7 @@ int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
   const long long t2 = mt_ub * ((p2.N + BN - 1) / BN);
   const int grid2 = int(t2 < sms ? t2 : sms);
   CUtensorMap mOut2;
-  if (!make_map(&mOut2, y_sorted, rows_h, c.d, 32)) return MOE_E_CUDA;
+  if (!make_bf16_map(&mOut2, y_sorted, rows_h, c.d, 32)) return MOE_E_CUDA;
   p2.tma_store = 1;
   grouped_gemm_kernel<false><<<grid2, THREADS, DYN_SMEM, st>>>(mA2, mA2, mA2h, mA2h, mB2, mOut2, p2);
   note_launches(2);
@@ -959,13 +986,13 @@ int launch_grouped_ffn_backward(const moe_cfg& c, const void* x_sorted, const vo
   if (!g1_saved) {
     CUtensorMap mA, mAh, mAs, mAsh, mB;
     const bool sx = c.has_shared;
-    if (!make_map(&mA, x_sorted, uint64_t(R), c.d, BM)) return MOE_E_CUDA;
-    if (!make_map(&mAh, x_sorted, uint64_t(R), c.d, BM / 2)) return MOE_E_CUDA;
-    if (!make_map(&mAs, sx ? x : x_sorted, sx ? uint64_t(c.T) : uint64_t(R), c.d, BM))
+    if (!make_bf16_map(&mA, x_sorted, uint64_t(R), c.d, BM)) return MOE_E_CUDA;
+    if (!make_bf16_map(&mAh, x_sorted, uint64_t(R), c.d, BM / 2)) return MOE_E_CUDA;
+    if (!make_bf16_map(&mAs, sx ? x : x_sorted, sx ? uint64_t(c.T) : uint64_t(R), c.d, BM))
       return MOE_E_CUDA;
-    if (!make_map(&mAsh, sx ? x : x_sorted, sx ? uint64_t(c.T) : uint64_t(R), c.d, BM / 2))
+    if (!make_bf16_map(&mAsh, sx ? x : x_sorted, sx ? uint64_t(c.T) : uint64_t(R), c.d, BM / 2))
       return MOE_E_CUDA;
-    if (!make_map(&mB, W13, uint64_t(n_exp) * 2 * c.f, c.d, BN)) return MOE_E_CUDA;
+    if (!make_bf16_map(&mB, W13, uint64_t(n_exp) * 2 * c.f, c.d, BN)) return MOE_E_CUDA;
     GroupedParams p = base;
     p.K = c.d;
     p.N = 2 * c.f;
@@ -975,7 +1002,7 @@ int launch_grouped_ffn_backward(const moe_cfg& c, const void* x_sorted, const vo
     p.out = g1w;
     p.ld_out = 2 * c.f;
     CUtensorMap mO;
-    if (!make_map(&mO, g1w, rows_h, 2 * c.f, 32)) return MOE_E_CUDA;
+    if (!make_bf16_map(&mO, g1w, rows_h, 2 * c.f, 32)) return MOE_E_CUDA;
     p.tma_store = 1;
     MOE_TRY_INTERNAL(launch_gg(rows_h, n_exp, mA, mAs, mAh, mAsh, mB, mO, p, st));
   }
@@ -983,9 +1010,9 @@ int launch_grouped_ffn_backward(const moe_cfg& c, const void* x_sorted, const vo
   //    SwiGLU derivative with g1 and writes dg1 (packed like W13)
   {
     CUtensorMap mA, mAh, mB;
-    if (!make_map(&mA, d_o, rows_h, c.d, BM)) return MOE_E_CUDA;
-    if (!make_map(&mAh, d_o, rows_h, c.d, BM / 2)) return MOE_E_CUDA;
-    if (!make_map(&mB, W2t, uint64_t(n_exp) * c.f, c.d, BN)) return MOE_E_CUDA;
+    if (!make_bf16_map(&mA, d_o, rows_h, c.d, BM)) return MOE_E_CUDA;
+    if (!make_bf16_map(&mAh, d_o, rows_h, c.d, BM / 2)) return MOE_E_CUDA;
+    if (!make_bf16_map(&mB, W2t, uint64_t(n_exp) * c.f, c.d, BN)) return MOE_E_CUDA;
     GroupedParams p = base;
     p.K = c.d;
     p.N = c.f;
@@ -1000,9 +1027,9 @@ int launch_grouped_ffn_backward(const moe_cfg& c, const void* x_sorted, const vo
   // 3. dx_sorted = dg1 W13 (B = W13^T per expert, N = d, K = 2f)
   {
     CUtensorMap mA, mAh, mB;
-    if (!make_map(&mA, dg1, rows_h, 2 * c.f, BM)) return MOE_E_CUDA;
-    if (!make_map(&mAh, dg1, rows_h, 2 * c.f, BM / 2)) return MOE_E_CUDA;
-    if (!make_map(&mB, W13t, uint64_t(n_exp) * c.d, 2 * c.f, BN)) return MOE_E_CUDA;
+    if (!make_bf16_map(&mA, dg1, rows_h, 2 * c.f, BM)) return MOE_E_CUDA;
+    if (!make_bf16_map(&mAh, dg1, rows_h, 2 * c.f, BM / 2)) return MOE_E_CUDA;
+    if (!make_bf16_map(&mB, W13t, uint64_t(n_exp) * c.d, 2 * c.f, BN)) return MOE_E_CUDA;
     GroupedParams p = base;
     p.K = 2 * c.f;
     p.N = c.d;
@@ -1011,7 +1038,7 @@ int launch_grouped_ffn_backward(const moe_cfg& c, const void* x_sorted, const vo
     p.out = static_cast<__nv_bfloat16*>(dx_sorted);
     p.ld_out = c.d;
     CUtensorMap mO;
-    if (!make_map(&mO, dx_sorted, rows_h, c.d, 32)) return MOE_E_CUDA;
+    if (!make_bf16_map(&mO, dx_sorted, rows_h, c.d, 32)) return MOE_E_CUDA;
     p.tma_store = 1;
     MOE_TRY_INTERNAL(launch_gg(rows_h, n_exp, mA, mA, mAh, mAh, mB, mO, p, st));
   }
@@ -1027,9 +1054,9 @@ int launch_grouped_ffn_backward(const moe_cfg& c, const void* x_sorted, const vo
   {
     // dW2[g] = d_o^T h: [d, f] per segment
     CUtensorMap mA, mAh, mB;
-    if (!make_map(&mA, trA, uint64_t(c.d), kub, BM)) return MOE_E_CUDA;
-    if (!make_map(&mAh, trA, uint64_t(c.d), kub, BM / 2)) return MOE_E_CUDA;
-    if (!make_map(&mB, trB, uint64_t(c.f), kub, BN)) return MOE_E_CUDA;
+    if (!make_bf16_map(&mA, trA, uint64_t(c.d), kub, BM)) return MOE_E_CUDA;
+    if (!make_bf16_map(&mAh, trA, uint64_t(c.d), kub, BM / 2)) return MOE_E_CUDA;
+    if (!make_bf16_map(&mB, trB, uint64_t(c.f), kub, BN)) return MOE_E_CUDA;
     GroupedParams p = base;
     p.K = BK;
     p.N = c.f;
@@ -1039,7 +1066,7 @@ int launch_grouped_ffn_backward(const moe_cfg& c, const void* x_sorted, const vo
     p.out = static_cast<__nv_bfloat16*>(dW2);
     p.ld_out = c.f;
     CUtensorMap mO;
-    if (!make_map(&mO, dW2, uint64_t(n_exp) * c.d, c.f, 32)) return MOE_E_CUDA;
+    if (!make_bf16_map(&mO, dW2, uint64_t(n_exp) * c.d, c.f, 32)) return MOE_E_CUDA;
     p.tma_store = 1;
     MOE_TRY_INTERNAL(launch_gg(int64_t(n_exp) * c.d, n_exp, mA, mA, mAh, mAh, mB, mO, p, st));
   }
@@ -1051,9 +1078,9 @@ int launch_grouped_ffn_backward(const moe_cfg& c, const void* x_sorted, const vo
   {
     // dW13[g] = dg1^T x: [2f, d] per segment (rows packed like W13)
     CUtensorMap mA, mAh, mB;
-    if (!make_map(&mA, trA, uint64_t(2 * c.f), kub, BM)) return MOE_E_CUDA;
-    if (!make_map(&mAh, trA, uint64_t(2 * c.f), kub, BM / 2)) return MOE_E_CUDA;
-    if (!make_map(&mB, trC, uint64_t(c.d), kub, BN)) return MOE_E_CUDA;
+    if (!make_bf16_map(&mA, trA, uint64_t(2 * c.f), kub, BM)) return MOE_E_CUDA;
+    if (!make_bf16_map(&mAh, trA, uint64_t(2 * c.f), kub, BM / 2)) return MOE_E_CUDA;
+    if (!make_bf16_map(&mB, trC, uint64_t(c.d), kub, BN)) return MOE_E_CUDA;
     GroupedParams p = base;
     p.K = BK;
     p.N = c.d;
@@ -1063,7 +1090,7 @@ int launch_grouped_ffn_backward(const moe_cfg& c, const void* x_sorted, const vo
     p.out = static_cast<__nv_bfloat16*>(dW13);
     p.ld_out = c.d;
     CUtensorMap mO;
-    if (!make_map(&mO, dW13, uint64_t(n_exp) * 2 * c.f, c.d, 32)) return MOE_E_CUDA;
+    if (!make_bf16_map(&mO, dW13, uint64_t(n_exp) * 2 * c.f, c.d, 32)) return MOE_E_CUDA;
     p.tma_store = 1;
     MOE_TRY_INTERNAL(launch_gg(int64_t(n_exp) * 2 * c.f, n_exp, mA, mA, mAh, mAh, mB, mO, p,
                                st));

@@ -65,6 +65,15 @@ int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
                        const int32_t* gather_order, const int32_t* counts, const int32_t* offsets,
                        const void* W13, const void* W2, void* h, void* y_sorted, void* g1,
                        void* ws, cudaStream_t st);
+// The forward FFN on SM pairs (two-CTA clusters, transposed tiles).
+int launch_grouped_ffn_pair(const moe_cfg& c, const void* x_sorted, const void* x,
+                            const int32_t* counts, const int32_t* offsets, const void* W13,
+                            const void* W2, void* h, void* y_sorted, int* status,
+                            cudaStream_t st);
+// 2-D bf16 row-major [rows, cols] tensor map, box = 64 columns x box_rows rows,
+// 128-byte swizzle, out-of-bounds elements read as zero (false on failure).
+bool make_bf16_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
+                   uint32_t box_rows);
 int launch_combine(const moe_cfg& c, const void* y_sorted, const int32_t* inv, const float* gate,
                    void* y, cudaStream_t st);
 

@@ -14,9 +14,9 @@ from __future__ import annotations
 
 import torch
 
-from . import (MoeCfg, moe_backward_workspace_bytes, moe_combine, moe_combine_backward,
+from . import (MoeCfg, MoeLayerBufs, moe_backward_workspace_bytes, moe_combine, moe_combine_backward,
                moe_ep_layout, moe_grouped_ffn, moe_grouped_ffn_backward, moe_grouped_ffn_gather,
-               moe_grouped_ffn_train,
+               moe_grouped_ffn_train, moe_layer_forward, moe_layer_forward_host,
                moe_grouped_rows, moe_last_launch_count, moe_pack_backward, moe_pack_router,
                moe_pack_w13, moe_permute, moe_permute_backward, moe_route, moe_router_logits,
                moe_workspace_bytes, moe_workspace_init)
@@ -180,6 +180,44 @@ class MoELayer:
         n, f2, d = self.dW13.shape
         blk = self.dW13.view(n, f2 // 256, 2, 128, d)
         return blk[:, :, 0].reshape(n, f2 // 2, d), blk[:, :, 1].reshape(n, f2 // 2, d)
+
+    def c_bufs(self) -> MoeLayerBufs:
+        """This layer's weights and buffers as the C struct moe_layer (the
+        router step included when the layer holds router weights)."""
+        if getattr(self, "_c_bufs", None) is None:
+            self._c_bufs = MoeLayerBufs.of(
+                W_r=self.W_r if self.W_r_split is None else None, W_r_split=self.W_r_split,
+                logit_bias=self.logit_bias, selection_bias=self.selection_bias, W13=self.W13,
+                W2=self.W2, scores=self.scores, topk_idx=self.topk_idx, topk_gate=self.topk_gate,
+                counts=self.counts, offsets=self.offsets, order=self.order, inv=self.inv,
+                x_sorted=self.x_sorted, count_mat=self.count_mat, send_off=self.send_off,
+                recv_off=self.recv_off, send_idx=self.send_idx, send_buf=self.send_buf,
+                h=self.h, y_sorted=self.y_sorted, ws=self.ws)
+        return self._c_bufs
+
+    def forward_c(self, x, y=None):
+        """The forward through the library's single entry point
+        moe_layer_forward (same steps as forward, issued from C)."""
+        if self.gather or self.train:
+            raise RuntimeError("moe_layer_forward runs the rows path's inference forward")
+        out = self.y if y is None else y
+        moe_layer_forward(self.cfg, self.c_bufs(), x, out)
+        self.launches_per_forward = moe_last_launch_count()
+        return out
+
+    def forward_host_c(self, x_hosts, y_hosts):
+        """forward_host_stream done by the library (moe_layer_forward_host):
+        pinned host batches in and out, one copy per direction per batch on
+        its own stream, double-buffered on the device, the forward issued
+        from C.  Returns once enqueued; synchronise the current stream to wait
+        for the last result."""
+        if self.gather or self.train:
+            raise RuntimeError("moe_layer_forward_host runs the rows path's inference forward")
+        s_in, s_out = self._copy_streams()
+        self._stream_buffers()
+        moe_layer_forward_host(self.cfg, self.c_bufs(), x_hosts, y_hosts, self._xbuf,
+                               self._ybuf, torch.cuda.current_stream(self.device), s_in, s_out)
+        return y_hosts
 
     def forward_host_stream(self, x_hosts, y_hosts):
         """Runs the layer on a sequence of host batches (pinned bf16 [T, d] each)

@@ -262,9 +262,16 @@ int moe_pack_w13(const moe_cfg* cfg, const moe_bf16* W1, const moe_bf16* W3,
  *             accumulation, rounded to bf16; shared expert rows at R + t
  *   y_sorted  bf16 [R + has_shared*T, d] out: h W2^T, fp32 accumulation
  * Rows outside the experts' kept rows are not written.  E + has_shared <= 1025.
- * The kernels are persistent (one CTA per SM); a device-side wait that exceeds
- * one second records MOE_E_DEVICE_TIMEOUT in the workspace status word and the
- * kernel returns early (outputs then incomplete). */
+ * The kernels are persistent (one CTA per SM, or one two-CTA cluster per SM
+ * pair); a device-side wait that exceeds one second records
+ * MOE_E_DEVICE_TIMEOUT in the workspace status word and the kernel returns
+ * early (outputs then incomplete).
+ * Tiles: layers whose expected rows per expert T*k/E (at most the capacity)
+ * reach 768 run on SM pairs (256 weight rows by up to 256 tokens per tile,
+ * tcgen05 cta_group::2); others on one-SM 128-row tiles.  The environment
+ * variable MOE_FFN_TILES = "pair" or "single" overrides the choice; it is read
+ * at every call.  Both give results within the layer's tolerance; they are not
+ * bit-identical to each other. */
 int moe_grouped_ffn(const moe_cfg* cfg, const moe_bf16* x_sorted, const moe_bf16* x,
                     const int32_t* counts, const int32_t* offsets,
                     const moe_bf16* W13, const moe_bf16* W2, moe_bf16* h,
@@ -294,6 +301,63 @@ int moe_grouped_ffn_gather(const moe_cfg* cfg, const moe_bf16* x, const int32_t*
  *   y        bf16 [T, d] out */
 int moe_combine(const moe_cfg* cfg, const moe_bf16* y_sorted, const int32_t* inv,
                 const float* topk_gate, moe_bf16* y, void* stream);
+
+/* ------------------------------------------------------------------------
+ * The whole forward in one call (the seven steps of "Expert parallelism" in
+ * order, as the step calls above run them).
+ * ------------------------------------------------------------------------ */
+
+/* The layer's weights and step buffers, all device pointers, each as the step
+ * call that takes it states. */
+typedef struct moe_layer {
+  const float* W_r;              /* fp32 [d, E]; NULL with W_r_split NULL: no router
+                                    step, `scores` already holds the scores */
+  const moe_bf16* W_r_split;     /* bf16 [3, E, d] (moe_pack_router) or NULL */
+  const float* logit_bias;       /* fp32 [E] or NULL */
+  const float* selection_bias;   /* fp32 [E] or NULL */
+  const moe_bf16* W13;           /* moe_pack_w13 */
+  const moe_bf16* W2;
+  float* scores;
+  int32_t* topk_idx;
+  float* topk_gate;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* order;
+  int32_t* inv;
+  moe_bf16* x_sorted;
+  int32_t* count_mat;
+  int32_t* send_off;
+  int32_t* recv_off;
+  int32_t* send_idx;
+  moe_bf16* send_buf;            /* or NULL: the layout without the packed rows */
+  moe_bf16* h;
+  moe_bf16* y_sorted;
+  void* ws;                      /* workspace of moe_workspace_bytes(cfg) bytes */
+  size_t ws_bytes;
+} moe_layer;
+
+/* The forward on device tokens x (bf16 [T, d]) into y (bf16 [T, d]):
+ * moe_router_logits (when L has router weights) -> moe_route -> moe_permute ->
+ * moe_ep_layout -> moe_grouped_ffn -> moe_combine, on `stream`.  Returns the
+ * first error of a step (nothing after it is launched). */
+int moe_layer_forward(const moe_cfg* cfg, const moe_layer* L, const moe_bf16* x, moe_bf16* y,
+                      void* stream);
+
+/* The forward on n_batches batches held in host memory:
+ *   x_host[i], y_host[i]  HOST pointers, bf16 [T, d] each, page-locked (for
+ *                         example cudaHostAlloc) so that the copies overlap
+ *   x_dev[0..1], y_dev[0..1]  two device buffers per side, bf16 [T, d]
+ * Batch i's host-to-device copy (one cudaMemcpyAsync on copy_in_stream) runs
+ * while batch i-1 computes on compute_stream, and batch i-1's device-to-host
+ * copy (one cudaMemcpyAsync on copy_out_stream, or copy_in_stream when NULL)
+ * while batch i computes; events order each buffer's reuse.  Returns once
+ * everything is enqueued: compute_stream completes after the last result has
+ * reached y_host.  The call creates and destroys its own events and allocates
+ * no memory. */
+int moe_layer_forward_host(const moe_cfg* cfg, const moe_layer* L, int n_batches,
+                           const moe_bf16* const* x_host, moe_bf16* const* y_host,
+                           moe_bf16* const* x_dev, moe_bf16* const* y_dev, void* compute_stream,
+                           void* copy_in_stream, void* copy_out_stream);
 
 /* ------------------------------------------------------------------------
  * Backward of the layer with the routing held fixed ("Expert parallelism":
