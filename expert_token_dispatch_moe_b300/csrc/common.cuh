@@ -15,18 +15,26 @@ namespace moe {
 // ---------------------------------------------------------------------------
 // Workspace layout (all regions 256-byte aligned)
 //   [0, 256)       status word (int32 at 0), finished-CTA counter of the
-//                  permute histogram (uint32 at 8, back to 0 after each call)
+//                  permute histogram (uint32 at 8, back to 0 after each call),
+//                  grid barrier of the one-launch permute: arrival count
+//                  (uint32 at 16, back to 0 after each barrier) and generation
+//                  (uint32 at 24, only grows)
 //   src_cnt        int32 [n_ep][E]   assignments per (source rank, expert)
 //   chunk_hist     int32 [n_chunks][E] per-chunk histogram, then chunk bases
+//   slice_hist     int32 [kFusedMaxCtas][E] per-CTA histograms of the one-launch
+//                  permute (E <= kFusedMaxE only)
 //   ep_sbase       int32 [n_ep][E]   (unused: the layout kernel keeps these bases in shared memory)
 //   send_pos       int32 [A]         send slot of each assignment (-1 dropped)
 //   router_part    fp32 [S][T][E]    partial logits of the tensor-core router when it
 //                                    splits K into S > 1 chunks (router_k_split)
 // ---------------------------------------------------------------------------
 constexpr int kPermChunk = 2048;   // assignments per histogram/rank CTA
+constexpr int kFusedMaxE = 64;     // the one-launch permute's largest expert count
+constexpr int kFusedMaxCtas = 512; // and its most CTAs
 
 struct WsLayout {
-  size_t status, done_ctas, src_cnt, chunk_hist, ep_sbase, send_pos, router_part, total;
+  size_t status, done_ctas, bar_count, bar_gen, src_cnt, chunk_hist, slice_hist, ep_sbase,
+      send_pos, router_part, total;
   int n_chunks;
 };
 
@@ -51,9 +59,12 @@ inline WsLayout ws_layout(const moe_cfg& c) {
   size_t A = size_t(c.T) * c.k;
   L.n_chunks = int((A + kPermChunk - 1) / kPermChunk);
   size_t off = 0;
-  L.status = off;     L.done_ctas = off + 8;  off += 256;
+  L.status = off;     L.done_ctas = off + 8;
+  L.bar_count = off + 16;  L.bar_gen = off + 24;  off += 256;
   L.src_cnt = off;    off += align256(size_t(c.n_ep) * c.E * 4);
   L.chunk_hist = off; off += align256(size_t(L.n_chunks) * c.E * 4);
+  L.slice_hist = off;
+  if (c.E <= kFusedMaxE) off += align256(size_t(kFusedMaxCtas) * c.E * 4);
   L.ep_sbase = off;   off += align256(size_t(c.n_ep) * c.E * 4);
   L.send_pos = off;   off += align256(A * 4);
   const int ks = router_k_split(c);

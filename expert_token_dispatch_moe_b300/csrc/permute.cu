@@ -4,7 +4,10 @@
 // "Token permutation and grouped GEMMs" (Expert parallelism page): order is
 // the stable argsort of the expert ids and inv[order] = arange.  The stable
 // rank of an assignment inside its expert comes from histograms and prefix
-// sums, never from the order of atomics, so every output is deterministic:
+// sums, never from the order of atomics, so every output is deterministic.
+// Three paths: up to 4096 assignments (and 256 experts), one CTA computes the
+// indices; up to 64 experts, one cooperative launch does everything
+// (perm_fused_kernel, below); otherwise:
 //   1. hist:  per 2048-assignment chunk, a histogram over experts (shared-memory
 //             atomics: only counts, not order, depend on them); counts per
 //             (source rank, expert) for the layout.  The CTA that finishes
@@ -326,8 +329,38 @@ __global__ void __launch_bounds__(kPermSmallThreads, 1) perm_index_small_kernel(
 }
 
 // ---------------------------------------------------------------------------
+// Row moves.  A warp copies one token row of vec 16-byte vectors to up to k
+// destination rows (lane j < k holds destination row j, or -1): it loads
+// 32*V vectors (V per lane) before storing any, so a row of up to 32*V
+// vectors costs one memory round trip.
+// ---------------------------------------------------------------------------
+template <int V>
+__device__ __forceinline__ void move_row(const uint4* __restrict__ src, int vec, int my_row,
+                                         int k, uint4* __restrict__ dst, int lane) {
+  for (int v0 = 0; v0 < vec; v0 += 32 * V) {
+    uint4 buf[V];
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const int v = v0 + u * 32 + lane;
+      if (v < vec) buf[u] = __ldg(src + v);
+    }
+    for (int j = 0; j < k; ++j) {
+      const int row = __shfl_sync(0xffffffffu, my_row, j);
+      if (row < 0) continue;
+      uint4* d = dst + size_t(row) * vec;
+#pragma unroll
+      for (int u = 0; u < V; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v < vec) d[v] = buf[u];
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // 3. row move: one warp per token, x[t] read once, written to its k rows.
 // ---------------------------------------------------------------------------
+template <int V>
 __global__ void __launch_bounds__(256) row_scatter_kernel(const uint4* __restrict__ x, int T,
                                                           int vec_per_row, int k,
                                                           const int32_t* __restrict__ rows,
@@ -336,26 +369,7 @@ __global__ void __launch_bounds__(256) row_scatter_kernel(const uint4* __restric
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
   const int my_row = (lane < k) ? __ldg(rows + size_t(t) * k + lane) : -1;
-  const uint4* src = x + size_t(t) * vec_per_row;
-  // warp-uniform trip count: every lane takes part in the row broadcasts
-  for (int v0 = 0; v0 < vec_per_row; v0 += 32 * 4) {
-    uint4 buf[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int v = v0 + u * 32 + lane;
-      if (v < vec_per_row) buf[u] = __ldg(src + v);
-    }
-    for (int j = 0; j < k; ++j) {
-      const int row = __shfl_sync(0xffffffffu, my_row, j);
-      if (row < 0) continue;
-      uint4* d = dst + size_t(row) * vec_per_row;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int v = v0 + u * 32 + lane;
-        if (v < vec_per_row) d[v] = buf[u];
-      }
-    }
-  }
+  move_row<V>(x + size_t(t) * vec_per_row, vec_per_row, my_row, k, dst, lane);
 }
 
 // Capacity mode: set the order entry of the grouped buffer's padding rows to
@@ -391,24 +405,30 @@ __global__ void __launch_bounds__(256) perm_pad_kernel(const int32_t* __restrict
 //                  = sum over q's experts of before[e] (or min(before[e], cap)).
 //
 // CTA (s, j) computes the tables of source rank s (every CTA of the rank
-// recomputes them; CTA (s, 0) writes them out) and then places the rank's
-// assignments j*kEpPerCta .. (j+1)*kEpPerCta - 1: slot(a) = sbase[s][e] +
-// rank(a) for each kept assignment a (send_pos[a], -1 when dropped;
-// send_idx[slot] = a), and marks the rank's slots past its kept rows empty
-// (send_idx = -1).
-constexpr int kEpPerCta = 1024;  // assignments placed per CTA
+// recomputes them; CTA (s, 0) writes them out) and then takes the rank's
+// assignments j*apc .. (j+1)*apc - 1 (apc a multiple of k, so whole tokens):
+// slot(a) = sbase[s][e] + rank(a) for each kept assignment a (send_pos[a], -1
+// when dropped; send_idx[slot] = a), marks the slots of that range past the
+// rank's kept rows empty (send_idx = -1), and, with a send buffer, moves its
+// tokens' rows to their slots (one warp per token, x[t] read once) and zeroes
+// the empty slots' rows.
+constexpr int kEpMaxPerCta = 2048;  // assignments placed per CTA at most
 
+template <int V>
 __global__ void __launch_bounds__(kPermThreads) ep_layout_kernel(
     const int32_t* __restrict__ src_cnt, const int32_t* __restrict__ idx,
     const int32_t* __restrict__ inv, const int32_t* __restrict__ offsets, int n_ep, int E, int k,
-    int T_loc, int capacity, int32_t* __restrict__ C, int32_t* __restrict__ send_off,
+    int T_loc, int capacity, int apc, int32_t* __restrict__ C, int32_t* __restrict__ send_off,
     int32_t* __restrict__ recv_off, int32_t* __restrict__ send_idx,
-    int32_t* __restrict__ send_pos) {
+    int32_t* __restrict__ send_pos, const uint4* __restrict__ x, int vec_per_row,
+    uint4* __restrict__ send_buf) {
   extern __shared__ int32_t sm[];
   int32_t* kept = sm;              // [E + 1] -> exclusive prefix
   int32_t* recv = sm + E + 1;      // [E + 1] -> exclusive prefix
   int32_t* bef = sm + 2 * (E + 1); // [E]
+  int32_t* slot_s = sm + 3 * E + 2;  // [apc]: slot of each assignment of the range
   const int s = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int b = 0, sp = 0;
     for (; sp + 4 <= s; sp += 4) {
@@ -441,9 +461,9 @@ __global__ void __launch_bounds__(kPermThreads) ep_layout_kernel(
   }
   const int rpr = T_loc * k;
   const int base = s * rpr;
-  for (int j = blockIdx.y; j * kEpPerCta < rpr; j += gridDim.y) {
-    const int i_end = min(rpr, (j + 1) * kEpPerCta);
-    for (int i = j * kEpPerCta + threadIdx.x; i < i_end; i += blockDim.x) {
+  for (int j = blockIdx.y; j * apc < rpr; j += gridDim.y) {
+    const int i0 = j * apc, i_end = min(rpr, i0 + apc);
+    for (int i = i0 + threadIdx.x; i < i_end; i += blockDim.x) {
       const int a = base + i;
       const int e = __ldg(idx + a);
       const int row = __ldg(inv + a);
@@ -453,27 +473,272 @@ __global__ void __launch_bounds__(kPermThreads) ep_layout_kernel(
         send_idx[p] = a;
       }
       send_pos[a] = p;
+      slot_s[i - i0] = p;
       if (i >= kept_all) send_idx[a] = -1;  // slot a is past the rank's kept rows
     }
+    if (send_buf == nullptr) continue;
+    __syncthreads();
+    // the range's token rows to their slots
+    for (int t = (base + i0) / k + warp; t < (base + i_end) / k; t += kPermThreads / 32) {
+      const int my_slot = lane < k ? slot_s[t * k - base - i0 + lane] : -1;
+      move_row<V>(x + size_t(t) * vec_per_row, vec_per_row, my_slot, k, send_buf, lane);
+    }
+    // empty slots of the range (past the rank's kept rows): zero rows
+    for (int i = max(i0, kept_all) + warp; i < i_end; i += kPermThreads / 32) {
+      uint4* d = send_buf + size_t(base + i) * vec_per_row;
+      for (int v = lane; v < vec_per_row; v += 32) d[v] = make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
   }
 }
 
-// Zero the send-buffer rows past each rank's kept rows (slot p of rank
-// s = p / rows_per_rank is empty when p - s*rows_per_rank >= its kept rows).
-// One warp per row, grid-stride.
-__global__ void __launch_bounds__(256) ep_pad_kernel(const int32_t* __restrict__ C,
-                                                     const int32_t* __restrict__ send_off,
-                                                     int n_ep, int rows_per_rank, int A,
-                                                     int vec_per_row,
-                                                     uint4* __restrict__ send_buf) {
-  const int lane = threadIdx.x & 31;
-  const int warps = (gridDim.x * blockDim.x) >> 5;
-  for (int p = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; p < A; p += warps) {
-    const int s = p / rows_per_rank;
-    const size_t last = size_t(s) * n_ep + n_ep - 1;
-    if (p - s * rows_per_rank < __ldg(send_off + last) + __ldg(C + last)) continue;
-    uint4* row = send_buf + size_t(p) * vec_per_row;
-    for (int v = lane; v < vec_per_row; v += 32) row[v] = make_uint4(0, 0, 0, 0);
+// ---------------------------------------------------------------------------
+// The whole permute in one cooperative launch, for layers with few experts
+// (E <= kFusedMaxE) and more assignments than the one-CTA path takes.  CTA c
+// owns tokens [c*tpc, (c+1)*tpc) and their assignments:
+//   1. it loads its expert ids, counts its slice per expert into
+//      slice_hist[c] (CTA 0 also clears the per-(rank, expert) counts), and
+//      meets the other CTAs at a grid barrier;
+//   2. from every CTA's histogram it takes its slice's base in each expert
+//      (the sum over earlier CTAs) and the expert totals, and from those the
+//      segment offsets (CTA 0 writes counts and offsets); then each warp starts
+//      loading its first rows (registers), which overlaps step 3;
+//   3. stable ranks inside the slice in index order (warp match/popc, then a
+//      scan over the 8 warps), giving inv and order; per-(rank, expert)
+//      counts by warp-aggregated atomics;
+//   4. capacity padding rows: order -1 and zero rows (grid-stride);
+//   5. its tokens' rows: one warp per token, x[t] written to its k rows, in
+//      4 KB chunks through two register buffers (load the next, store this).
+// The grid barrier is bounded: after 1 s it records MOE_E_DEVICE_TIMEOUT and
+// lets the CTA continue (outputs then unreliable, never a hang).
+// ---------------------------------------------------------------------------
+constexpr int kFusedThreads = 256;
+constexpr int kFusedRounds = 8;        // 2048 assignments per CTA at most
+constexpr int kFusedChunk = 8;         // 16-byte vectors per lane in each row buffer
+
+__device__ __forceinline__ unsigned int ld_volatile_u32(const unsigned int* p) {
+  return *reinterpret_cast<const volatile unsigned int*>(p);
+}
+
+// The CTA's last thread arrives and waits; its fence waits for that thread's
+// own outstanding memory operations, so it must have no slow loads in flight.
+__device__ void grid_barrier(unsigned int* count, unsigned int* gen, int* status) {
+  __syncthreads();
+  if (threadIdx.x == blockDim.x - 1) {
+    const unsigned int g = ld_volatile_u32(gen);
+    __threadfence();
+    if (atomicAdd(count, 1u) == gridDim.x - 1) {
+      atomicExch(count, 0u);
+      __threadfence();
+      atomicAdd(gen, 1u);
+    } else {
+      const uint64_t t0 = global_ns();
+      while (ld_volatile_u32(gen) == g) {
+        if (global_ns() - t0 > 1000000000ull) {
+          report_status(status, MOE_E_DEVICE_TIMEOUT);
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kFusedThreads) perm_fused_kernel(
+    const int32_t* __restrict__ idx, const uint4* __restrict__ x, int T, int E, int k, int T_loc,
+    int n_ep, int capacity, int tpc, int vec_per_row, int32_t* __restrict__ slice_hist,
+    int32_t* __restrict__ src_cnt, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ inv, int32_t* __restrict__ order, uint4* __restrict__ x_sorted,
+    int* status, unsigned int* bar_count, unsigned int* bar_gen) {
+  __shared__ int32_t h[kFusedMaxE];          // slice histogram, then running rank base
+  __shared__ int32_t tot[kFusedMaxE];        // expert totals
+  __shared__ int32_t seg[kFusedMaxE + 1];    // segment offsets (dropless)
+  __shared__ int32_t wcnt[kFusedThreads / 32][kFusedMaxE];
+  __shared__ int32_t rows_s[kFusedRounds * kFusedThreads];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t lt = (1u << lane) - 1u;
+  const int c = blockIdx.x;
+  const int t0 = c * tpc, t1 = min(T, t0 + tpc);
+  const int n_a = t1 > t0 ? (t1 - t0) * k : 0;
+  const int a0 = t0 * k;
+
+  // 1. ids, the first token row of each warp, the slice histogram
+  for (int e = tid; e < E; e += kFusedThreads) h[e] = 0;
+  if (c == 0)
+    for (int i = tid; i < n_ep * E; i += kFusedThreads) src_cnt[i] = 0;
+  int ev[kFusedRounds];
+#pragma unroll
+  for (int r = 0; r < kFusedRounds; ++r) {
+    const int i = r * kFusedThreads + tid;
+    ev[r] = i < n_a ? __ldg(idx + a0 + i) : -1;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < kFusedRounds; ++r) {
+    if (r * kFusedThreads >= n_a) break;
+    const int i = r * kFusedThreads + tid;
+    int e = ev[r];
+    if (i < n_a && (e < 0 || e >= E)) {
+      report_status(status, MOE_E_DEVICE_DATA);
+      e = -1;
+    }
+    ev[r] = e;
+    const uint32_t pe = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && (pe & lt) == 0) atomicAdd(&h[e], __popc(pe));
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kFusedThreads) slice_hist[size_t(c) * E + e] = h[e];
+  // the row loads go out only now, behind the id loads and the histogram, so
+  // that they overlap the barrier and steps 2-3 rather than delay them
+  // The warp's rows move as a sequence of items of up to 32 * kFusedChunk
+  // vectors (its tokens t0 + warp, t0 + warp + 8, ..., each cut into cpr
+  // chunks), through two register buffers: the next item loads while the
+  // current one is stored.
+  uint4 buf_a[kFusedChunk], buf_b[kFusedChunk];
+  const int cpr = (vec_per_row + 32 * kFusedChunk - 1) / (32 * kFusedChunk);
+  const int my_tokens = t1 > t0 + warp ? (t1 - t0 - warp + kFusedThreads / 32 - 1) /
+                                             (kFusedThreads / 32) : 0;
+  const int n_items = x_sorted != nullptr ? my_tokens * cpr : 0;
+  auto load_item = [&](uint4 (&b)[kFusedChunk], int it) {
+    const int t = t0 + warp + (it / cpr) * (kFusedThreads / 32);
+    const int v0 = (it % cpr) * 32 * kFusedChunk;
+    const uint4* src = x + size_t(t) * vec_per_row + v0;
+#pragma unroll
+    for (int u = 0; u < kFusedChunk; ++u)
+      if (v0 + u * 32 + lane < vec_per_row) b[u] = __ldg(src + u * 32 + lane);
+  };
+  grid_barrier(bar_count, bar_gen, status);
+
+  // 2. the slice's base in each expert, expert totals, segment offsets
+  {
+    int P = 32;  // threads per expert (a power of two, P * E <= kFusedThreads)
+    while (P > 1 && P * E > kFusedThreads) P >>= 1;
+    const int e = tid / P, p = tid - e * P;
+    int before = 0, total = 0;
+    if (e < E) {
+#pragma unroll 4
+      for (int cc = p; cc < int(gridDim.x); cc += P) {
+        const int v = __ldcg(slice_hist + size_t(cc) * E + e);
+        total += v;
+        if (cc < c) before += v;
+      }
+    }
+    for (int off = P >> 1; off > 0; off >>= 1) {
+      before += __shfl_xor_sync(0xffffffffu, before, off);
+      total += __shfl_xor_sync(0xffffffffu, total, off);
+    }
+    if (e < E && p == 0) {
+      h[e] = before;
+      tot[e] = total;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int e0 = 2 * lane;
+    const int v0 = e0 < E ? tot[e0] : 0, v1 = e0 + 1 < E ? tot[e0 + 1] : 0;
+    int incl = v0 + v1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    const int excl = incl - v0 - v1;
+    if (e0 < E) seg[e0] = excl;
+    if (e0 + 1 < E) seg[e0 + 1] = excl + v0;
+    if (lane == 31) seg[E] = incl;
+  }
+  __syncthreads();
+  if (c == 0) {
+    for (int e = tid; e < E; e += kFusedThreads) {
+      counts[e] = tot[e];
+      offsets[e] = capacity ? e * capacity : seg[e];
+    }
+    if (tid == 0) offsets[E] = capacity ? E * capacity : seg[E];
+  }
+
+  // the first two row items load now: behind the small loads of steps 1-2
+  // (which would otherwise queue behind them), overlapping step 3
+  if (n_items > 0) load_item(buf_a, 0);
+  if (n_items > 1) load_item(buf_b, 1);
+
+  // 3. stable ranks inside the slice, rows, per-(rank, expert) counts
+#pragma unroll
+  for (int r = 0; r < kFusedRounds; ++r) {
+    if (r * kFusedThreads >= n_a) break;
+    const int i = r * kFusedThreads + tid;
+    const int a = a0 + i;
+    const int e = ev[r];
+    for (int q = tid; q < (kFusedThreads / 32) * E; q += kFusedThreads) wcnt[q / E][q % E] = 0;
+    __syncthreads();
+    const uint32_t pe = __match_any_sync(0xffffffffu, e);
+    const int lrank = __popc(pe & lt);
+    if (e >= 0 && lrank == 0) wcnt[warp][e] = __popc(pe);
+    __syncthreads();
+    if (tid < E) {
+      int run = h[tid];
+#pragma unroll
+      for (int w = 0; w < kFusedThreads / 32; ++w) {
+        const int v = wcnt[w][tid];
+        wcnt[w][tid] = run;
+        run += v;
+      }
+      h[tid] = run;
+    }
+    __syncthreads();
+    int row = -1;
+    if (e >= 0) {
+      const int rank = wcnt[warp][e] + lrank;
+      if (capacity) row = rank < capacity ? e * capacity + rank : -1;
+      else row = seg[e] + rank;
+    }
+    if (i < n_a) {
+      inv[a] = row;
+      if (row >= 0) order[row] = a;
+      rows_s[i] = row;
+    }
+    const int key = e >= 0 ? ((a / k) / T_loc) * E + e : -1;
+    const uint32_t pk = __match_any_sync(0xffffffffu, key);
+    if (key >= 0 && (pk & lt) == 0) atomicAdd(src_cnt + key, __popc(pk));
+    __syncthreads();
+  }
+
+  // 4. capacity padding rows
+  if (capacity) {
+    const int R = E * capacity;
+    const int gw = (c * kFusedThreads + tid) >> 5, nw = (gridDim.x * kFusedThreads) >> 5;
+    for (int rr = gw; rr < R; rr += nw) {
+      const int e = rr / capacity;
+      if (rr - e * capacity < min(tot[e], capacity)) continue;
+      if (lane == 0) order[rr] = -1;
+      if (x_sorted == nullptr) continue;
+      uint4* dst = x_sorted + size_t(rr) * vec_per_row;
+      for (int v = lane; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+    }
+  }
+
+  // 5. the slice's token rows, one warp per token, item by item
+  if (x_sorted == nullptr) return;
+  auto store_item = [&](const uint4 (&b)[kFusedChunk], int it) {
+    const int t = t0 + warp + (it / cpr) * (kFusedThreads / 32);
+    const int v0 = (it % cpr) * 32 * kFusedChunk;
+    const int my_row = lane < k ? rows_s[(t - t0) * k + lane] : -1;
+    for (int j = 0; j < k; ++j) {
+      const int row = __shfl_sync(0xffffffffu, my_row, j);
+      if (row < 0) continue;
+      uint4* d = x_sorted + size_t(row) * vec_per_row + v0;
+#pragma unroll
+      for (int u = 0; u < kFusedChunk; ++u)
+        if (v0 + u * 32 + lane < vec_per_row) d[u * 32 + lane] = b[u];
+    }
+  };
+  for (int it = 0; it < n_items; it += 2) {
+    store_item(buf_a, it);
+    if (it + 2 < n_items) load_item(buf_a, it + 2);
+    if (it + 1 < n_items) {
+      store_item(buf_b, it + 1);
+      if (it + 3 < n_items) load_item(buf_b, it + 3);
+    }
   }
 }
 
@@ -490,10 +755,81 @@ static int row_grid(long long rows) {
 int launch_row_scatter(const void* x, int T, int d, int k, const int32_t* rows, void* dst,
                        cudaStream_t st) {
   const int vec = d / 8;  // 16-byte vectors per row
-  row_scatter_kernel<<<(T + 7) / 8, 256, 0, st>>>(static_cast<const uint4*>(x), T, vec, k, rows,
-                                                 static_cast<uint4*>(dst));
+  // vectors per lane loaded before any store: rows of up to 256 vectors fit 8
+  // (fewer registers, more warps per SM); longer rows take 16 at a time
+  if (vec <= 256)
+    row_scatter_kernel<8><<<(T + 7) / 8, 256, 0, st>>>(static_cast<const uint4*>(x), T, vec, k,
+                                                      rows, static_cast<uint4*>(dst));
+  else
+    row_scatter_kernel<16><<<(T + 7) / 8, 256, 0, st>>>(static_cast<const uint4*>(x), T, vec, k,
+                                                       rows, static_cast<uint4*>(dst));
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_E_CUDA;
+}
+
+// CTAs of perm_fused_kernel that fit on the device at once (cached per device).
+static int fused_resident_ctas() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (cache[dev] == 0) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, perm_fused_kernel,
+                                                      kFusedThreads, 0) != cudaSuccess) {
+      cudaGetLastError();
+      per_sm = 0;
+    }
+    int coop = 0;
+    if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess) {
+      cudaGetLastError();
+      coop = 0;
+    }
+    cache[dev] = coop ? per_sm * device_sm_count() : -1;
+  }
+  return cache[dev];
+}
+
+// The one-launch permute; MOE_E_SHAPE when the batch needs more than one wave of
+// CTAs (the caller then takes the multi-launch path).
+static int launch_permute_fused(const moe_cfg& c, const void* x, const int32_t* idx,
+                                int32_t* counts, int32_t* offsets, int32_t* order, int32_t* inv,
+                                void* x_sorted, void* ws, cudaStream_t st) {
+  const int resident = fused_resident_ctas();
+  if (resident <= 0) return MOE_E_SHAPE;
+  // at most two CTAs per SM: more CTAs cost more in the barrier and in step 2
+  // than they add to the row moves (measured: Mixtral-shaped permute 23 against
+  // 26 us with three per SM)
+  int g_max = resident < 2 * device_sm_count() ? resident : 2 * device_sm_count();
+  if (g_max > kFusedMaxCtas) g_max = kFusedMaxCtas;
+  int tpc = (c.T + g_max - 1) / g_max;
+  if (tpc * c.k > kFusedRounds * kFusedThreads) return MOE_E_SHAPE;
+  int grid = (c.T + tpc - 1) / tpc;
+  const WsLayout L = ws_layout(c);
+  const int32_t* idx_p = idx;
+  const uint4* x_p = static_cast<const uint4*>(x);
+  int T = c.T, E = c.E, k = c.k, T_loc = c.T / c.n_ep, n_ep = c.n_ep, cap = c.capacity;
+  int vec = c.d / 8;
+  int32_t* slice_hist = ws_ptr<int32_t>(ws, L.slice_hist);
+  int32_t* src_cnt = ws_ptr<int32_t>(ws, L.src_cnt);
+  uint4* xs = static_cast<uint4*>(x_sorted);
+  int* status = ws_ptr<int>(ws, L.status);
+  unsigned int* bar_count = ws_ptr<unsigned int>(ws, L.bar_count);
+  unsigned int* bar_gen = ws_ptr<unsigned int>(ws, L.bar_gen);
+  void* args[] = {&idx_p, &x_p, &T, &E, &k, &T_loc, &n_ep, &cap, &tpc, &vec, &slice_hist,
+                  &src_cnt, &counts, &offsets, &inv, &order, &xs, &status, &bar_count,
+                  &bar_gen};
+  const cudaError_t e = cudaLaunchCooperativeKernel(
+      reinterpret_cast<const void*>(perm_fused_kernel), dim3(grid), dim3(kFusedThreads), args,
+      0, st);
+  note_launches(1);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_E_CUDA;
+  }
+  return MOE_OK;
 }
 
 int launch_permute(const moe_cfg& c, const void* x, const int32_t* idx, int32_t* counts,
@@ -505,6 +841,10 @@ int launch_permute(const moe_cfg& c, const void* x, const int32_t* idx, int32_t*
   unsigned int* done = ws_ptr<unsigned int>(ws, L.done_ctas);
   int32_t* src_cnt = ws_ptr<int32_t>(ws, L.src_cnt);
   int32_t* chunk_hist = ws_ptr<int32_t>(ws, L.chunk_hist);
+  if (A > kPermSmallMaxA && c.E <= kFusedMaxE && c.k <= 32) {
+    const int rc = launch_permute_fused(c, x, idx, counts, offsets, order, inv, x_sorted, ws, st);
+    if (rc != MOE_E_SHAPE) return rc;   // MOE_E_SHAPE: the batch does not fit one wave
+  }
   if (A <= kPermSmallMaxA && c.E <= kPermSmallMaxE) {
     // one CTA does the histogram, the scans and the ranks
     static PerDeviceOnce once;
@@ -547,27 +887,30 @@ int launch_ep_layout(const moe_cfg& c, const int32_t* idx, const int32_t* offset
                      int32_t* send_idx, const void* x, void* send_buf, void* ws,
                      cudaStream_t st) {
   const WsLayout L = ws_layout(c);
-  const int A = c.T * c.k;
   const int T_loc = c.T / c.n_ep;
   int32_t* src_cnt = ws_ptr<int32_t>(ws, L.src_cnt);
   int32_t* send_pos = ws_ptr<int32_t>(ws, L.send_pos);
-  const size_t smem = size_t(3 * c.E + 2) * 4;
-  const int per_rank = (T_loc * c.k + kEpPerCta - 1) / kEpPerCta;
+  const bool rows = x && send_buf;
+  // assignments per CTA: whole tokens; when rows move, one token per warp (as
+  // many rows in flight as a plain scatter), else up to kEpMaxPerCta
+  int tok_per_cta = rows ? kPermThreads / 32 : kEpMaxPerCta / c.k;
+  if (tok_per_cta < 1) tok_per_cta = 1;
+  const int apc = tok_per_cta * c.k;
+  const int per_rank = (T_loc * c.k + apc - 1) / apc;
+  const size_t smem = size_t(3 * c.E + 2 + apc) * 4;
   const dim3 grid(c.n_ep, per_rank < 65535 ? per_rank : 65535);
-  ep_layout_kernel<<<grid, kPermThreads, smem, st>>>(src_cnt, idx, inv, offsets, c.n_ep, c.E,
-                                                       c.k, T_loc, c.capacity, C, send_off,
-                                                       recv_off, send_idx, send_pos);
+  const uint4* xr = static_cast<const uint4*>(rows ? x : nullptr);
+  uint4* sb = static_cast<uint4*>(rows ? send_buf : nullptr);
+  if (c.d / 8 <= 256)
+    ep_layout_kernel<8><<<grid, kPermThreads, smem, st>>>(
+        src_cnt, idx, inv, offsets, c.n_ep, c.E, c.k, T_loc, c.capacity, apc, C, send_off,
+        recv_off, send_idx, send_pos, xr, c.d / 8, sb);
+  else
+    ep_layout_kernel<16><<<grid, kPermThreads, smem, st>>>(
+        src_cnt, idx, inv, offsets, c.n_ep, c.E, c.k, T_loc, c.capacity, apc, C, send_off,
+        recv_off, send_idx, send_pos, xr, c.d / 8, sb);
   note_launches(1);
-  if (cudaGetLastError() != cudaSuccess) return MOE_E_CUDA;
-  if (x && send_buf) {
-    if (c.capacity) {
-      ep_pad_kernel<<<row_grid(A), 256, 0, st>>>(C, send_off, c.n_ep, T_loc * c.k, A, c.d / 8,
-                                                 static_cast<uint4*>(send_buf));
-      note_launches(1);
-    }
-    return launch_row_scatter(x, c.T, c.d, c.k, send_pos, send_buf, st);
-  }
-  return MOE_OK;
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_E_CUDA;
 }
 
 }  // namespace moe

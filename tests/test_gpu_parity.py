@@ -148,6 +148,52 @@ def test_permute_and_layout_parity(m, name):
     _check_permute(cfg, x_dev, idx_np, out, lay)
 
 
+# Batches that take the one-launch permute (more than 4096 assignments, at
+# most 64 experts): ragged slices, expert counts that are not powers of two,
+# k up to 8, capacity drops, a single expert, and a batch too large for one
+# wave of CTAs (it falls back to the multi-launch path).
+ONE_LAUNCH = {
+    "e8_ragged": C["tiny"].with_(name="e8_ragged", T=3000, E=8, k=2, n_ep=4, d=256),
+    "e48_k3": C["tiny"].with_(name="e48_k3", T=5000, E=48, k=3, n_ep=4, d=128),
+    "e64_k8": C["tiny"].with_(name="e64_k8", T=4104, E=64, k=8, n_ep=8, d=64),
+    "e16_cap": C["tiny"].with_(name="e16_cap", T=6000, E=16, k=2, n_ep=4, d=192, capacity=600),
+    "e1": C["tiny"].with_(name="e1", T=5000, E=1, k=1, n_ep=1, d=64),
+    "fallback": C["tiny"].with_(name="fallback", T=80000, E=8, k=8, n_ep=8, d=64),
+}
+
+
+@pytest.mark.parametrize("name", list(ONE_LAUNCH))
+def test_permute_one_launch_parity(m, name):
+    cfg = ONE_LAUNCH[name]
+    scores = synth.make_scores(cfg, seed=31)
+    idx_np = oracle.select_experts(scores.numpy(), cfg.k, None, cfg.n_groups, cfg.topk_groups)
+    x_dev = synth.make_x(cfg, device="cuda", seed=32)
+    for _ in range(2):   # twice in a row: the grid barrier's words return to their start
+        out, lay = _permute_case(m, cfg, x_dev, idx_np)
+        _check_permute(cfg, x_dev, idx_np, out, lay)
+
+
+def test_permute_one_launch_indices_only(m):
+    cfg = ONE_LAUNCH["e16_cap"]
+    scores = synth.make_scores(cfg, seed=33)
+    idx_np = oracle.select_experts(scores.numpy(), cfg.k)
+    c = m.MoeCfg.from_layer(cfg)
+    i32 = torch.int32
+    counts = torch.empty(cfg.E, dtype=i32, device="cuda")
+    offsets = torch.empty(cfg.E + 1, dtype=i32, device="cuda")
+    order = torch.empty(cfg.R, dtype=i32, device="cuda")
+    inv = torch.empty(cfg.A, dtype=i32, device="cuda")
+    ws = torch.zeros(m.moe_workspace_bytes(c), dtype=torch.uint8, device="cuda")
+    m.moe_workspace_init(c, ws)
+    idx = torch.from_numpy(idx_np.astype(np.int32)).cuda()
+    m.moe_permute(c, None, idx, counts, offsets, order, inv, None, ws)
+    torch.cuda.synchronize()
+    ref = oracle.permute(idx_np, cfg.E, cfg.capacity)
+    for key, t in (("counts", counts), ("offsets", offsets), ("order", order), ("inv", inv)):
+        assert np.array_equal(npi(t), ref[key]), key
+    assert m.moe_get_device_status(ws) == 0
+
+
 def test_hand_dispatch_on_gpu(m):
     """The pages' two-GPU hand example, run through the CUDA path."""
     import json, os
@@ -174,13 +220,15 @@ def test_hot_expert_capacity_drops(m):
     _check_permute(cfg, x_dev, idx_np, out, lay)
 
 
-@pytest.mark.parametrize("T", [64, 2500])   # one-CTA index kernel, and the multi-CTA path
-def test_bad_expert_id_is_reported(m, T):
-    cfg = C["tiny"].with_(T=T, E=8, k=2, n_ep=2, d=64)
+# T = 64: the one-CTA index kernel; 2500: the one-launch permute; 2500 with
+# 80 experts: the multi-launch path
+@pytest.mark.parametrize("T,E", [(64, 8), (2500, 8), (2500, 80)])
+def test_bad_expert_id_is_reported(m, T, E):
+    cfg = C["tiny"].with_(T=T, E=E, k=2, n_ep=2, d=64)
     c = m.MoeCfg.from_layer(cfg)
     idx = torch.zeros(cfg.T, cfg.k, dtype=torch.int32)
     idx[:, 1] = 1
-    idx[5, 0] = 8
+    idx[5, 0] = E
     idx[9, 1] = -1
     x = synth.make_x(cfg, device="cuda")
     i32 = torch.int32
@@ -218,7 +266,8 @@ def test_layer_parity_small(m, name):
     out_ref = oracle.expert_outputs(x.float().numpy(), st["perm"], cfg.k, W1.float().numpy(),
                                     W3.float().numpy(), W2.float().numpy())
     kept = np.nonzero(st["perm"]["order"] >= 0)[0]
-    assert_y_close(npf(layer.y_sorted[:cfg.R]), out_ref, rows=kept)
+    # kept rows only: capacity padding rows of y_sorted are never written
+    assert_y_close(npf(layer.y_sorted[torch.from_numpy(kept).cuda()]), out_ref[kept])
     assert_y_close(npf(layer.y), y_ref)
     assert m.moe_get_device_status(layer.ws) == 0
 
