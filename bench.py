@@ -369,10 +369,11 @@ def _time_fp8_and_balance(m, layer, c, cfg, x, st, flush, counts, pk, reps, time
 
 
 def _kernel_source_digest():
-    """sha1 over the sources of the grouped GEMM (its kernel and PTX wrappers)."""
+    """sha1 over the sources of the grouped GEMMs (both kernels and the PTX wrappers)."""
     import hashlib
     h = hashlib.sha1()
     for rel in ("expert_token_dispatch_moe_b300/csrc/grouped_ffn.cu",
+                "expert_token_dispatch_moe_b300/csrc/grouped_pair.cu",
                 "expert_token_dispatch_moe_b300/csrc/common.cuh"):
         with open(os.path.join(ROOT, rel), "rb") as fh:
             h.update(fh.read())

@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -21,7 +22,7 @@ namespace moe {
 //                  (uint32 at 24, only grows)
 //   src_cnt        int32 [n_ep][E]   assignments per (source rank, expert)
 //   chunk_hist     int32 [n_chunks][E] per-chunk histogram, then chunk bases
-//   slice_hist     int32 [kFusedMaxCtas][E] per-CTA histograms of the one-launch
+//   slice_hist     int32 [E][CTAs] per-CTA histograms of the one-launch
 //                  permute (E <= kFusedMaxE only)
 //   ep_sbase       int32 [n_ep][E]   (unused: the layout kernel keeps these bases in shared memory)
 //   send_pos       int32 [A]         send slot of each assignment (-1 dropped)
@@ -99,6 +100,14 @@ __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w &
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low 16 bits)
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Four fp32 values as e4m3 codes (round to nearest even, saturated at 448),
+// packed low to high.
+__device__ __forceinline__ uint32_t fp8x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
 }
 
 // ---------------------------------------------------------------------------

@@ -57,9 +57,12 @@ int launch_route(const moe_cfg& c, const float* scores, const float* bias, int32
 int launch_permute(const moe_cfg& c, const void* x, const int32_t* idx, int32_t* counts,
                    int32_t* offsets, int32_t* order, int32_t* inv, void* x_sorted, void* ws,
                    cudaStream_t st);
+// The EP layout; with x and send_buf, the bf16 send rows; with x, send_fp8 and
+// send_scale (send_buf NULL), the e4m3 send rows and their scales.
 int launch_ep_layout(const moe_cfg& c, const int32_t* idx, const int32_t* offsets,
                      const int32_t* inv, int32_t* C, int32_t* send_off, int32_t* recv_off,
-                     int32_t* send_idx, const void* x, void* send_buf, void* ws, cudaStream_t st);
+                     int32_t* send_idx, const void* x, void* send_buf, void* ws, cudaStream_t st,
+                     void* send_fp8 = nullptr, float* send_scale = nullptr);
 int launch_pack_w13(const moe_cfg& c, const void* W1, const void* W3, void* W13, cudaStream_t st);
 int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
                        const int32_t* gather_order, const int32_t* counts, const int32_t* offsets,
@@ -87,8 +90,6 @@ int launch_eplb_dispatch(const moe_cfg& c, const int32_t* idx, const int32_t* in
                          const int32_t* copy_offset, const int32_t* copy_rank, int32_t* dest,
                          int32_t* C, cudaStream_t st);
 
-int launch_fp8_pack(const moe_cfg& c, const void* x, const int32_t* send_idx, void* send_fp8,
-                    float* send_scale, void* ws, cudaStream_t st);
 int launch_fp8_recv(const moe_cfg& c, const void* send_fp8, const float* send_scale,
                     const int32_t* send_idx, const int32_t* inv, void* x_sorted, cudaStream_t st);
 

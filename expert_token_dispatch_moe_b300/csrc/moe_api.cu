@@ -209,9 +209,8 @@ MOE_API int moe_ep_layout_fp8(const moe_cfg* c, const int32_t* topk_idx, const i
   MOE_TRY(check_ws(c, ws, ws_bytes));
   MOE_TRY(device_ok());
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  MOE_TRY(launch_ep_layout(*c, topk_idx, offsets, inv, count_mat, send_off, recv_off, send_idx,
-                           nullptr, nullptr, ws, st));
-  return launch_fp8_pack(*c, x, send_idx, send_fp8, send_scale, ws, st);
+  return launch_ep_layout(*c, topk_idx, offsets, inv, count_mat, send_off, recv_off, send_idx, x,
+                          nullptr, ws, st, send_fp8, send_scale);
 }
 
 MOE_API int moe_dispatch_recv_fp8(const moe_cfg* c, const uint8_t* send_fp8,

@@ -357,6 +357,69 @@ __device__ __forceinline__ void move_row(const uint4* __restrict__ src, int vec,
   }
 }
 
+// The FP8 form of move_row: the row's absmax (warp reduction), then its e4m3
+// codes (8 per 16-byte vector of bf16) and the row's scale written to each
+// destination row.  scale = absmax / 448 and the factor 448 / absmax are one
+// correctly rounded division each (1 for an all-zero row); each code is one
+// fp32 product and one conversion.  A row of up to 32*V vectors stays in
+// registers between the two passes; a longer one is read twice (the second
+// time from L1/L2).
+template <int V>
+__device__ __forceinline__ void quantize_row(const uint4* __restrict__ src, int vec, int my_row,
+                                             int k, uint2* __restrict__ dst_codes,
+                                             float* __restrict__ dst_scale, int lane) {
+  uint4 buf[V];
+  float amax = 0.0f;
+  for (int v0 = 0; v0 < vec; v0 += 32 * V) {
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const int v = v0 + u * 32 + lane;
+      buf[u] = v < vec ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const uint32_t w[4] = {buf[u].x, buf[u].y, buf[u].z, buf[u].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        amax = fmaxf(amax, fmaxf(fabsf(bf16lo(w[i])), fabsf(bf16hi(w[i]))));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  const float inv = amax > 0.0f ? __fdiv_rn(448.0f, amax) : 1.0f;
+  if (lane < k && my_row >= 0) dst_scale[my_row] = scale;
+  const bool one_pass = vec <= 32 * V;
+  for (int v0 = 0; v0 < vec; v0 += 32 * V) {
+    if (!one_pass) {
+#pragma unroll
+      for (int u = 0; u < V; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v < vec) buf[u] = __ldg(src + v);
+      }
+    }
+    uint2 code[V];
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const uint4 w = buf[u];
+      code[u].x = fp8x4(__fmul_rn(bf16lo(w.x), inv), __fmul_rn(bf16hi(w.x), inv),
+                        __fmul_rn(bf16lo(w.y), inv), __fmul_rn(bf16hi(w.y), inv));
+      code[u].y = fp8x4(__fmul_rn(bf16lo(w.z), inv), __fmul_rn(bf16hi(w.z), inv),
+                        __fmul_rn(bf16lo(w.w), inv), __fmul_rn(bf16hi(w.w), inv));
+    }
+    for (int j = 0; j < k; ++j) {
+      const int row = __shfl_sync(0xffffffffu, my_row, j);
+      if (row < 0) continue;
+      uint2* d = dst_codes + size_t(row) * vec;
+#pragma unroll
+      for (int u = 0; u < V; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v < vec) d[v] = code[u];
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // 3. row move: one warp per token, x[t] read once, written to its k rows.
 // ---------------------------------------------------------------------------
@@ -414,14 +477,15 @@ __global__ void __launch_bounds__(256) perm_pad_kernel(const int32_t* __restrict
 // the empty slots' rows.
 constexpr int kEpMaxPerCta = 2048;  // assignments placed per CTA at most
 
-template <int V>
+template <int V, bool FP8>
 __global__ void __launch_bounds__(kPermThreads) ep_layout_kernel(
     const int32_t* __restrict__ src_cnt, const int32_t* __restrict__ idx,
     const int32_t* __restrict__ inv, const int32_t* __restrict__ offsets, int n_ep, int E, int k,
     int T_loc, int capacity, int apc, int32_t* __restrict__ C, int32_t* __restrict__ send_off,
     int32_t* __restrict__ recv_off, int32_t* __restrict__ send_idx,
     int32_t* __restrict__ send_pos, const uint4* __restrict__ x, int vec_per_row,
-    uint4* __restrict__ send_buf) {
+    uint4* __restrict__ send_buf, uint2* __restrict__ send_fp8,
+    float* __restrict__ send_scale) {
   extern __shared__ int32_t sm[];
   int32_t* kept = sm;              // [E + 1] -> exclusive prefix
   int32_t* recv = sm + E + 1;      // [E + 1] -> exclusive prefix
@@ -476,17 +540,28 @@ __global__ void __launch_bounds__(kPermThreads) ep_layout_kernel(
       slot_s[i - i0] = p;
       if (i >= kept_all) send_idx[a] = -1;  // slot a is past the rank's kept rows
     }
-    if (send_buf == nullptr) continue;
+    if (x == nullptr) continue;
     __syncthreads();
-    // the range's token rows to their slots
+    // the range's token rows to their slots (bf16, or e4m3 codes and a scale)
     for (int t = (base + i0) / k + warp; t < (base + i_end) / k; t += kPermThreads / 32) {
       const int my_slot = lane < k ? slot_s[t * k - base - i0 + lane] : -1;
-      move_row<V>(x + size_t(t) * vec_per_row, vec_per_row, my_slot, k, send_buf, lane);
+      if (FP8)
+        quantize_row<V>(x + size_t(t) * vec_per_row, vec_per_row, my_slot, k, send_fp8,
+                        send_scale, lane);
+      else
+        move_row<V>(x + size_t(t) * vec_per_row, vec_per_row, my_slot, k, send_buf, lane);
     }
-    // empty slots of the range (past the rank's kept rows): zero rows
+    // empty slots of the range (past the rank's kept rows): zero rows (codes
+    // and scale 0 in FP8)
     for (int i = max(i0, kept_all) + warp; i < i_end; i += kPermThreads / 32) {
-      uint4* d = send_buf + size_t(base + i) * vec_per_row;
-      for (int v = lane; v < vec_per_row; v += 32) d[v] = make_uint4(0, 0, 0, 0);
+      if (FP8) {
+        if (lane == 0) send_scale[base + i] = 0.0f;
+        uint2* d = send_fp8 + size_t(base + i) * vec_per_row;
+        for (int v = lane; v < vec_per_row; v += 32) d[v] = make_uint2(0, 0);
+      } else {
+        uint4* d = send_buf + size_t(base + i) * vec_per_row;
+        for (int v = lane; v < vec_per_row; v += 32) d[v] = make_uint4(0, 0, 0, 0);
+      }
     }
     __syncthreads();
   }
@@ -588,7 +663,9 @@ __global__ void __launch_bounds__(kFusedThreads) perm_fused_kernel(
     if (e >= 0 && (pe & lt) == 0) atomicAdd(&h[e], __popc(pe));
   }
   __syncthreads();
-  for (int e = tid; e < E; e += kFusedThreads) slice_hist[size_t(c) * E + e] = h[e];
+  // expert-major table [E][gridDim.x], so that step 2 reads each expert's
+  // column as contiguous words
+  for (int e = tid; e < E; e += kFusedThreads) slice_hist[size_t(e) * gridDim.x + c] = h[e];
   // the row loads go out only now, behind the id loads and the histogram, so
   // that they overlap the barrier and steps 2-3 rather than delay them
   // The warp's rows move as a sequence of items of up to 32 * kFusedChunk
@@ -619,7 +696,7 @@ __global__ void __launch_bounds__(kFusedThreads) perm_fused_kernel(
     if (e < E) {
 #pragma unroll 4
       for (int cc = p; cc < int(gridDim.x); cc += P) {
-        const int v = __ldcg(slice_hist + size_t(cc) * E + e);
+        const int v = __ldcg(slice_hist + size_t(e) * gridDim.x + cc);
         total += v;
         if (cc < c) before += v;
       }
@@ -884,13 +961,14 @@ int launch_permute(const moe_cfg& c, const void* x, const int32_t* idx, int32_t*
 
 int launch_ep_layout(const moe_cfg& c, const int32_t* idx, const int32_t* offsets,
                      const int32_t* inv, int32_t* C, int32_t* send_off, int32_t* recv_off,
-                     int32_t* send_idx, const void* x, void* send_buf, void* ws,
-                     cudaStream_t st) {
+                     int32_t* send_idx, const void* x, void* send_buf, void* ws, cudaStream_t st,
+                     void* send_fp8, float* send_scale) {
   const WsLayout L = ws_layout(c);
   const int T_loc = c.T / c.n_ep;
   int32_t* src_cnt = ws_ptr<int32_t>(ws, L.src_cnt);
   int32_t* send_pos = ws_ptr<int32_t>(ws, L.send_pos);
-  const bool rows = x && send_buf;
+  const bool fp8 = x && send_fp8 && send_scale;
+  const bool rows = fp8 || (x && send_buf);
   // assignments per CTA: whole tokens; when rows move, one token per warp (as
   // many rows in flight as a plain scatter), else up to kEpMaxPerCta
   int tok_per_cta = rows ? kPermThreads / 32 : kEpMaxPerCta / c.k;
@@ -900,15 +978,26 @@ int launch_ep_layout(const moe_cfg& c, const int32_t* idx, const int32_t* offset
   const size_t smem = size_t(3 * c.E + 2 + apc) * 4;
   const dim3 grid(c.n_ep, per_rank < 65535 ? per_rank : 65535);
   const uint4* xr = static_cast<const uint4*>(rows ? x : nullptr);
-  uint4* sb = static_cast<uint4*>(rows ? send_buf : nullptr);
-  if (c.d / 8 <= 256)
-    ep_layout_kernel<8><<<grid, kPermThreads, smem, st>>>(
-        src_cnt, idx, inv, offsets, c.n_ep, c.E, c.k, T_loc, c.capacity, apc, C, send_off,
-        recv_off, send_idx, send_pos, xr, c.d / 8, sb);
-  else
-    ep_layout_kernel<16><<<grid, kPermThreads, smem, st>>>(
-        src_cnt, idx, inv, offsets, c.n_ep, c.E, c.k, T_loc, c.capacity, apc, C, send_off,
-        recv_off, send_idx, send_pos, xr, c.d / 8, sb);
+  uint4* sb = static_cast<uint4*>(rows && !fp8 ? send_buf : nullptr);
+  uint2* sf = static_cast<uint2*>(fp8 ? send_fp8 : nullptr);
+  float* ss = fp8 ? send_scale : nullptr;
+  const int vec = c.d / 8;
+#define MOE_EP_LAYOUT(V_, F_)                                                                   \
+  ep_layout_kernel<V_, F_><<<grid, kPermThreads, smem, st>>>(                                 \
+      src_cnt, idx, inv, offsets, c.n_ep, c.E, c.k, T_loc, c.capacity, apc, C, send_off,       \
+      recv_off, send_idx, send_pos, xr, vec, sb, sf, ss)
+  // vectors per lane held at once: rows of up to 256 vectors take 8 (62
+  // registers, four CTAs per SM); longer rows take 16 (one memory round trip
+  // for a 4096-wide row: the Mixtral-shaped layout ran 22 against 24 us, in
+  // spite of fewer warps per SM)
+  if (fp8) {
+    if (vec <= 256) MOE_EP_LAYOUT(8, true);
+    else MOE_EP_LAYOUT(16, true);
+  } else {
+    if (vec <= 256) MOE_EP_LAYOUT(8, false);
+    else MOE_EP_LAYOUT(16, false);
+  }
+#undef MOE_EP_LAYOUT
   note_launches(1);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_E_CUDA;
 }
