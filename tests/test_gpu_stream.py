@@ -12,12 +12,16 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("graphs", [False, True])
-@pytest.mark.parametrize("name,n", [("tiny", 5), ("mixtral", 3), ("dsv3_decode", 3)])
+@pytest.mark.parametrize("name,n", [("tiny", 5), ("mixtral", 3), ("dsv3_decode", 3), ("skew", 3)])
 def test_forward_host_stream_matches_device_forward(name, n, graphs):
     import expert_token_dispatch_moe_b300 as m
     cfg = synth.CONFIGS[name]
     if name == "mixtral":
         cfg = cfg.with_(T=512)   # the full expert shapes, fewer tokens
+    if name == "skew":
+        # 5120 assignments over 64 experts: the one-launch (cooperative) permute,
+        # captured in the graphs too
+        cfg = cfg.with_(T=2560, capacity=100)
     W1, W3, W2 = synth.make_expert_weights(cfg, device="cuda")
     W_r, lb = synth.make_router(cfg, device="cuda")
     layer = m.MoELayer(cfg, W1, W3, W2, W_r=W_r, logit_bias=lb)
