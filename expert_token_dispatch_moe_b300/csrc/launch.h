@@ -19,6 +19,9 @@ void note_launches(int n);
 // Multiprocessors of the current device (cached per device; 148 if unknown).
 int device_sm_count();
 
+// MOE_OK when the current device is an sm_103 part, else MOE_E_DEVICE.
+int device_ok();
+
 // A set-up step whose effect belongs to one device, such as a kernel's opt-in
 // to more than 48 KB of dynamic shared memory (cudaFuncSetAttribute applies to
 // the current device only): run(step) calls step() with the caller's device

@@ -81,6 +81,9 @@ MOE_API int moe_layer_forward_host(const moe_cfg* c, const moe_layer* L, int n_b
   }
   for (int i = 0; i < n_batches; ++i)
     if (!x_host[i] || !y_host[i]) return MOE_E_NULL;
+  if (n_batches == 0) return MOE_OK;
+  const int dev_rc = device_ok();
+  if (dev_rc != MOE_OK) return dev_rc;
   cudaStream_t comp = static_cast<cudaStream_t>(compute_stream);
   cudaStream_t s_in = static_cast<cudaStream_t>(copy_in_stream);
   cudaStream_t s_out = copy_out_stream ? static_cast<cudaStream_t>(copy_out_stream) : s_in;

@@ -39,7 +39,7 @@ static int64_t rows_R(const moe_cfg& c) {
 }
 
 // Is the current device an sm_103 part?  Cached per device ordinal.
-static int device_ok() {
+int device_ok() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
     cudaGetLastError();

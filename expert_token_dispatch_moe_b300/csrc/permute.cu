@@ -574,17 +574,20 @@ __global__ void __launch_bounds__(kPermThreads) ep_layout_kernel(
 //   1. it loads its expert ids, counts its slice per expert into
 //      slice_hist[c] (CTA 0 also clears the per-(rank, expert) counts), and
 //      meets the other CTAs at a grid barrier;
-//   2. from every CTA's histogram it takes its slice's base in each expert
-//      (the sum over earlier CTAs) and the expert totals, and from those the
-//      segment offsets (CTA 0 writes counts and offsets); then each warp starts
-//      loading its first rows (registers), which overlaps step 3;
+//   2. its slice's base in each expert (the sum over earlier CTAs) and the
+//      expert totals: read directly from the whole table when it is small
+//      (up to 16 words per thread), else from per-expert column scans (CTA e
+//      scans expert e's column into exclusive prefixes and writes the total
+//      to counts[e]) behind a second grid barrier; then the totals are
+//      scanned into the segment offsets (CTA 0 writes them);
 //   3. stable ranks inside the slice in index order (warp match/popc, then a
 //      scan over the 8 warps), giving inv and order; per-(rank, expert)
-//      counts by warp-aggregated atomics;
+//      counts by warp-aggregated atomics; then each warp starts loading its
+//      first rows (registers);
 //   4. capacity padding rows: order -1 and zero rows (grid-stride);
 //   5. its tokens' rows: one warp per token, x[t] written to its k rows, in
 //      4 KB chunks through two register buffers (load the next, store this).
-// The grid barrier is bounded: after 1 s it records MOE_E_DEVICE_TIMEOUT and
+// The grid barriers are bounded: after 1 s one records MOE_E_DEVICE_TIMEOUT and
 // lets the CTA continue (outputs then unreliable, never a hang).
 // ---------------------------------------------------------------------------
 constexpr int kFusedThreads = 256;
@@ -687,8 +690,13 @@ __global__ void __launch_bounds__(kFusedThreads) perm_fused_kernel(
   };
   grid_barrier(bar_count, bar_gen, status);
 
-  // 2. the slice's base in each expert, expert totals, segment offsets
-  {
+  // 2. the slice's base in each expert and the expert totals.  A small table
+  // (at most 16 words per thread) is read whole by every CTA, its threads
+  // split over the experts; a larger one is scanned column by column: CTA e
+  // turns expert e's column into exclusive prefixes in place and writes the
+  // total to counts[e], and after a second barrier every CTA reads its own
+  // base in each expert.  (The condition is the same in every CTA.)
+  if (E * int(gridDim.x) <= 16 * kFusedThreads) {
     int P = 32;  // threads per expert (a power of two, P * E <= kFusedThreads)
     while (P > 1 && P * E > kFusedThreads) P >>= 1;
     const int e = tid / P, p = tid - e * P;
@@ -708,6 +716,22 @@ __global__ void __launch_bounds__(kFusedThreads) perm_fused_kernel(
     if (e < E && p == 0) {
       h[e] = before;
       tot[e] = total;
+      if (c == 0) counts[e] = total;
+    }
+  } else {
+    for (int e = c; e < E; e += gridDim.x) {
+      int32_t* col = slice_hist + size_t(e) * gridDim.x;
+      for (int i = tid; i < int(gridDim.x); i += kFusedThreads) rows_s[i] = __ldcg(col + i);
+      __syncthreads();
+      const int total = block_exclusive_scan(rows_s, gridDim.x);
+      for (int i = tid; i < int(gridDim.x); i += kFusedThreads) col[i] = rows_s[i];
+      if (tid == 0) counts[e] = total;
+      __syncthreads();
+    }
+    grid_barrier(bar_count, bar_gen, status);
+    for (int e = tid; e < E; e += kFusedThreads) {
+      h[e] = __ldcg(slice_hist + size_t(e) * gridDim.x + c);
+      tot[e] = __ldcg(counts + e);
     }
   }
   __syncthreads();
@@ -727,17 +751,9 @@ __global__ void __launch_bounds__(kFusedThreads) perm_fused_kernel(
   }
   __syncthreads();
   if (c == 0) {
-    for (int e = tid; e < E; e += kFusedThreads) {
-      counts[e] = tot[e];
-      offsets[e] = capacity ? e * capacity : seg[e];
-    }
+    for (int e = tid; e < E; e += kFusedThreads) offsets[e] = capacity ? e * capacity : seg[e];
     if (tid == 0) offsets[E] = capacity ? E * capacity : seg[E];
   }
-
-  // the first two row items load now: behind the small loads of steps 1-2
-  // (which would otherwise queue behind them), overlapping step 3
-  if (n_items > 0) load_item(buf_a, 0);
-  if (n_items > 1) load_item(buf_b, 1);
 
   // 3. stable ranks inside the slice, rows, per-(rank, expert) counts
 #pragma unroll
@@ -779,6 +795,12 @@ __global__ void __launch_bounds__(kFusedThreads) perm_fused_kernel(
     if (key >= 0 && (pk & lt) == 0) atomicAdd(src_cnt + key, __popc(pk));
     __syncthreads();
   }
+
+  // the first two row items load now, behind the small loads and stores of
+  // steps 1-3 (which queue behind row loads issued earlier: a timestamp probe
+  // put steps 2 and 3 at 4 us each with the loads in flight)
+  if (n_items > 0) load_item(buf_a, 0);
+  if (n_items > 1) load_item(buf_b, 1);
 
   // 4. capacity padding rows
   if (capacity) {

@@ -353,7 +353,7 @@ int moe_layer_forward(const moe_cfg* cfg, const moe_layer* L, const moe_bf16* x,
  * while batch i computes; events order each buffer's reuse.  Returns once
  * everything is enqueued: compute_stream completes after the last result has
  * reached y_host.  The call creates and destroys its own events and allocates
- * no memory. */
+ * no memory.  n_batches = 0 does nothing; a negative n_batches is MOE_E_SHAPE. */
 int moe_layer_forward_host(const moe_cfg* cfg, const moe_layer* L, int n_batches,
                            const moe_bf16* const* x_host, moe_bf16* const* y_host,
                            moe_bf16* const* x_dev, moe_bf16* const* y_dev, void* compute_stream,

@@ -109,6 +109,37 @@ def test_host_argument_errors(m):
         assert lib.moe_strerror(code)
 
 
+def test_layer_entry_points_host_errors(m):
+    """moe_layer_forward and moe_layer_forward_host check their arguments on the
+    host; without an sm_103 GPU a valid call fails with MOE_E_DEVICE."""
+    import torch
+    lib = m._lib
+    c = m.MoeCfg.from_layer(synth.CONFIGS["tiny"])
+    cfg = ctypes.byref(c)
+    P = 1 << 20
+    bufs = m.MoeLayerBufs()
+    for name, _ in m.MoeLayerBufs._fields_[:-1]:
+        setattr(bufs, name, P)
+    bufs.ws_bytes = m.moe_workspace_bytes(c)
+    lb = ctypes.byref(bufs)
+    arr = (ctypes.c_void_p * 2)(P, P)
+    assert lib.moe_layer_forward(cfg, None, P, P, None) == -1
+    assert lib.moe_layer_forward_host(cfg, None, 1, arr, arr, arr, arr, None, None, None) == -1
+    assert lib.moe_layer_forward_host(cfg, lb, 1, None, arr, arr, arr, None, None, None) == -1
+    assert lib.moe_layer_forward_host(cfg, lb, 2, (ctypes.c_void_p * 2)(P, None), arr, arr, arr,
+                                      None, None, None) == -1
+    assert lib.moe_layer_forward_host(cfg, lb, 1, arr, arr, (ctypes.c_void_p * 2)(P, P + 4),
+                                      arr, None, None, None) == -3
+    assert lib.moe_layer_forward_host(cfg, lb, -1, arr, arr, arr, arr, None, None, None) == -2
+    assert lib.moe_layer_forward_host(cfg, lb, 0, arr, arr, arr, arr, None, None, None) == 0
+    bad = m.MoeCfg.from_layer(synth.CONFIGS["tiny"].with_(E=7))
+    assert lib.moe_layer_forward_host(ctypes.byref(bad), lb, 1, arr, arr, arr, arr, None, None,
+                                      None) == -2
+    if not torch.cuda.is_available():
+        assert lib.moe_layer_forward(cfg, lb, P, P, None) == -6
+        assert lib.moe_layer_forward_host(cfg, lb, 1, arr, arr, arr, arr, None, None, None) == -6
+
+
 def _k_split(T, E, d):
     """The router's K-split rule restated: the largest divisor S of d/64 with at
     least 8 k-blocks per chunk and at most 148 output tiles in all."""
