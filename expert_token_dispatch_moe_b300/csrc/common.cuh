@@ -19,11 +19,15 @@ namespace moe {
 //                  permute histogram (uint32 at 8, back to 0 after each call),
 //                  grid barrier of the one-launch permute: arrival count
 //                  (uint32 at 16, back to 0 after each barrier) and generation
-//                  (uint32 at 24, only grows)
+//                  (uint32 at 24, only grows); launch sequence number of
+//                  the one-launch permute (uint32 at 32, only grows)
+//   grp_sums       int32 [2][kFusedMaxE][kFusedMaxGroups] at a fixed offset
+//                  (256): the one-launch permute's per-group slice counts, one
+//                  buffer per launch parity; each launch clears the other one
 //   src_cnt        int32 [n_ep][E]   assignments per (source rank, expert)
 //   chunk_hist     int32 [n_chunks][E] per-chunk histogram, then chunk bases
-//   slice_hist     int32 [E][CTAs] per-CTA histograms of the one-launch
-//                  permute (E <= kFusedMaxE only)
+//   slice_hist     int32 [E][kFusedMaxCtas] per-CTA histograms of the
+//                  one-launch permute (E <= kFusedMaxE only)
 //   ep_sbase       int32 [n_ep][E]   (unused: the layout kernel keeps these bases in shared memory)
 //   send_pos       int32 [A]         send slot of each assignment (-1 dropped)
 //   router_part    fp32 [S][T][E]    partial logits of the tensor-core router when it
@@ -32,10 +36,13 @@ namespace moe {
 constexpr int kPermChunk = 2048;   // assignments per histogram/rank CTA
 constexpr int kFusedMaxE = 64;     // the one-launch permute's largest expert count
 constexpr int kFusedMaxCtas = 512; // and its most CTAs
+constexpr int kFusedGroupCtas = 16; // CTAs per group of its slice-count sums
+constexpr int kFusedMaxGroups = kFusedMaxCtas / kFusedGroupCtas;
+constexpr size_t kWsHeadBytes = 256 + size_t(2) * kFusedMaxE * kFusedMaxGroups * 4;  // cleared by init
 
 struct WsLayout {
-  size_t status, done_ctas, bar_count, bar_gen, src_cnt, chunk_hist, slice_hist, ep_sbase,
-      send_pos, router_part, total;
+  size_t status, done_ctas, bar_count, bar_gen, perm_seq, grp_sums, src_cnt, chunk_hist,
+      slice_hist, ep_sbase, send_pos, router_part, total;
   int n_chunks;
 };
 
@@ -61,7 +68,8 @@ inline WsLayout ws_layout(const moe_cfg& c) {
   L.n_chunks = int((A + kPermChunk - 1) / kPermChunk);
   size_t off = 0;
   L.status = off;     L.done_ctas = off + 8;
-  L.bar_count = off + 16;  L.bar_gen = off + 24;  off += 256;
+  L.bar_count = off + 16;  L.bar_gen = off + 24;  L.perm_seq = off + 32;  off += 256;
+  L.grp_sums = off;   off = kWsHeadBytes;
   L.src_cnt = off;    off += align256(size_t(c.n_ep) * c.E * 4);
   L.chunk_hist = off; off += align256(size_t(L.n_chunks) * c.E * 4);
   L.slice_hist = off;

@@ -125,7 +125,7 @@ MOE_API int moe_workspace_init(const moe_cfg* c, void* ws, size_t ws_bytes, void
   MOE_TRY(moe_validate_cfg(c));
   MOE_TRY(check_ws(c, ws, ws_bytes));
   MOE_TRY(device_ok());
-  if (cudaMemsetAsync(ws, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  if (cudaMemsetAsync(ws, 0, kWsHeadBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MOE_E_CUDA;
   return MOE_OK;
 }

@@ -573,13 +573,14 @@ __global__ void __launch_bounds__(kPermThreads) ep_layout_kernel(
 // owns tokens [c*tpc, (c+1)*tpc) and their assignments:
 //   1. it loads its expert ids, counts its slice per expert into
 //      slice_hist[c] (CTA 0 also clears the per-(rank, expert) counts), and
-//      meets the other CTAs at a grid barrier;
+//      meets the other CTAs at a grid barrier; when the table (E x CTAs) is
+//      large it also adds the counts into its group's sums (groups of
+//      kFusedGroupCtas CTAs);
 //   2. its slice's base in each expert (the sum over earlier CTAs) and the
-//      expert totals: read directly from the whole table when it is small
-//      (up to 16 words per thread), else from per-expert column scans (CTA e
-//      scans expert e's column into exclusive prefixes and writes the total
-//      to counts[e]) behind a second grid barrier; then the totals are
-//      scanned into the segment offsets (CTA 0 writes them);
+//      expert totals: read from the whole table when it is small, else from
+//      the earlier groups' sums plus the counts of the earlier CTAs of its own
+//      group (totals: all groups' sums); then the totals are scanned into the
+//      segment offsets (CTA 0 writes them);
 //   3. stable ranks inside the slice in index order (warp match/popc, then a
 //      scan over the 8 warps), giving inv and order; per-(rank, expert)
 //      counts by warp-aggregated atomics; then each warp starts loading its
@@ -593,6 +594,7 @@ __global__ void __launch_bounds__(kPermThreads) ep_layout_kernel(
 constexpr int kFusedThreads = 256;
 constexpr int kFusedRounds = 8;        // 2048 assignments per CTA at most
 constexpr int kFusedChunk = 8;         // 16-byte vectors per lane in each row buffer
+constexpr int kFusedDirectWords = 16 * kFusedThreads;  // slice tables read whole up to this size
 
 __device__ __forceinline__ unsigned int ld_volatile_u32(const unsigned int* p) {
   return *reinterpret_cast<const volatile unsigned int*>(p);
@@ -628,7 +630,8 @@ __global__ void __launch_bounds__(kFusedThreads) perm_fused_kernel(
     int n_ep, int capacity, int tpc, int vec_per_row, int32_t* __restrict__ slice_hist,
     int32_t* __restrict__ src_cnt, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
     int32_t* __restrict__ inv, int32_t* __restrict__ order, uint4* __restrict__ x_sorted,
-    int* status, unsigned int* bar_count, unsigned int* bar_gen) {
+    int* status, unsigned int* bar_count, unsigned int* bar_gen, unsigned int* seq_word,
+    int32_t* __restrict__ grp_sums) {
   __shared__ int32_t h[kFusedMaxE];          // slice histogram, then running rank base
   __shared__ int32_t tot[kFusedMaxE];        // expert totals
   __shared__ int32_t seg[kFusedMaxE + 1];    // segment offsets (dropless)
@@ -640,8 +643,15 @@ __global__ void __launch_bounds__(kFusedThreads) perm_fused_kernel(
   const int t0 = c * tpc, t1 = min(T, t0 + tpc);
   const int n_a = t1 > t0 ? (t1 - t0) * k : 0;
   const int a0 = t0 * k;
+  // every CTA reads the sequence number before the barrier, CTA 0 advances it
+  // after: this launch adds into buffer seq & 1 (zero on entry) and clears the
+  // other buffer for the next launch
+  const unsigned int seq = ld_volatile_u32(seq_word);
+  constexpr int kGrpBuf = kFusedMaxE * kFusedMaxGroups;
+  int32_t* gsum = grp_sums + (seq & 1u) * kGrpBuf;
+  const int q = c / kFusedGroupCtas;  // the CTA's group
 
-  // 1. ids, the first token row of each warp, the slice histogram
+  // 1. ids, the slice histogram and the group sums
   for (int e = tid; e < E; e += kFusedThreads) h[e] = 0;
   if (c == 0)
     for (int i = tid; i < n_ep * E; i += kFusedThreads) src_cnt[i] = 0;
@@ -666,9 +676,15 @@ __global__ void __launch_bounds__(kFusedThreads) perm_fused_kernel(
     if (e >= 0 && (pe & lt) == 0) atomicAdd(&h[e], __popc(pe));
   }
   __syncthreads();
-  // expert-major table [E][gridDim.x], so that step 2 reads each expert's
-  // column as contiguous words
-  for (int e = tid; e < E; e += kFusedThreads) slice_hist[size_t(e) * gridDim.x + c] = h[e];
+  // expert-major table [E][kFusedMaxCtas], so that step 2 reads each
+  // expert's words as contiguous, 16-byte aligned runs; with a large table
+  // the counts also go into the group sums [E][kFusedMaxGroups]
+  const bool direct = E * int(gridDim.x) <= kFusedDirectWords;  // the same in every CTA
+  for (int e = tid; e < E; e += kFusedThreads) {
+    const int v = h[e];
+    slice_hist[e * kFusedMaxCtas + c] = v;
+    if (!direct && v) atomicAdd(gsum + e * kFusedMaxGroups + q, v);
+  }
   // the row loads go out only now, behind the id loads and the histogram, so
   // that they overlap the barrier and steps 2-3 rather than delay them
   // The warp's rows move as a sequence of items of up to 32 * kFusedChunk
@@ -690,23 +706,71 @@ __global__ void __launch_bounds__(kFusedThreads) perm_fused_kernel(
   };
   grid_barrier(bar_count, bar_gen, status);
 
-  // 2. the slice's base in each expert and the expert totals.  A small table
-  // (at most 16 words per thread) is read whole by every CTA, its threads
-  // split over the experts; a larger one is scanned column by column: CTA e
-  // turns expert e's column into exclusive prefixes in place and writes the
-  // total to counts[e], and after a second barrier every CTA reads its own
-  // base in each expert.  (The condition is the same in every CTA.)
-  if (E * int(gridDim.x) <= 16 * kFusedThreads) {
+  if (c == 0 && !direct) {
+    if (tid == 0) *seq_word = seq + 1u;
+    int32_t* other = grp_sums + ((seq + 1u) & 1u) * kGrpBuf;
+    for (int i = tid; i < kGrpBuf / 4; i += kFusedThreads)
+      reinterpret_cast<int4*>(other)[i] = make_int4(0, 0, 0, 0);
+  }
+
+  // 2. the slice's base in each expert and the expert totals, read by P
+  // threads per expert in one round of loads: from the whole table when it
+  // is small (16-byte loads), else from the sums of the earlier groups plus
+  // the counts of the group's earlier CTAs (at most kFusedMaxGroups +
+  // kFusedGroupCtas words per expert; the totals are the sums of all groups)
+  {
     int P = 32;  // threads per expert (a power of two, P * E <= kFusedThreads)
     while (P > 1 && P * E > kFusedThreads) P >>= 1;
     const int e = tid / P, p = tid - e * P;
     int before = 0, total = 0;
-    if (e < E) {
-#pragma unroll 4
-      for (int cc = p; cc < int(gridDim.x); cc += P) {
-        const int v = __ldcg(slice_hist + size_t(e) * gridDim.x + cc);
-        total += v;
-        if (cc < c) before += v;
+    if (direct) {
+      // E * gridDim.x <= kFusedDirectWords and P > kFusedThreads / (2E) bound
+      // the 16-byte words per thread by kDirectMax
+      constexpr int kDirectMax = kFusedDirectWords / (4 * (kFusedThreads / 2));
+      const int n4 = (int(gridDim.x) + 3) / 4;
+      int4 v[kDirectMax];
+      if (e < E) {
+        const int4* row = reinterpret_cast<const int4*>(slice_hist + e * kFusedMaxCtas);
+#pragma unroll
+        for (int i = 0; i < kDirectMax; ++i) {
+          const int j = p + i * P;
+          v[i] = j < n4 ? __ldcg(row + j) : make_int4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < kDirectMax; ++i) {
+          const int w = 4 * (p + i * P);  // first CTA of the word
+          const int g = int(gridDim.x);
+          const int x0 = w < g ? v[i].x : 0, x1 = w + 1 < g ? v[i].y : 0;
+          const int x2 = w + 2 < g ? v[i].z : 0, x3 = w + 3 < g ? v[i].w : 0;
+          total += x0 + x1 + x2 + x3;
+          before += (w < c ? x0 : 0) + (w + 1 < c ? x1 : 0) + (w + 2 < c ? x2 : 0) +
+                    (w + 3 < c ? x3 : 0);
+        }
+      }
+    } else {
+      const int nq = (int(gridDim.x) + kFusedGroupCtas - 1) / kFusedGroupCtas;
+      const int c_first = q * kFusedGroupCtas;
+      const int n_words = nq + (c - c_first);
+      constexpr int kMaxWords = (kFusedMaxGroups + kFusedGroupCtas + 3) / 4;  // P >= 4
+      int v[kMaxWords];
+      if (e < E) {
+        const int32_t* gs = gsum + e * kFusedMaxGroups;
+        const int32_t* hs = slice_hist + e * kFusedMaxCtas;
+#pragma unroll
+        for (int i = 0; i < kMaxWords; ++i) {
+          const int j = p + i * P;
+          v[i] = j < nq ? __ldcg(gs + j) : (j < n_words ? __ldcg(hs + (c_first + j - nq)) : 0);
+        }
+#pragma unroll
+        for (int i = 0; i < kMaxWords; ++i) {
+          const int j = p + i * P;
+          if (j < nq) {
+            total += v[i];
+            if (j < q) before += v[i];
+          } else {
+            before += v[i];
+          }
+        }
       }
     }
     for (int off = P >> 1; off > 0; off >>= 1) {
@@ -717,21 +781,6 @@ __global__ void __launch_bounds__(kFusedThreads) perm_fused_kernel(
       h[e] = before;
       tot[e] = total;
       if (c == 0) counts[e] = total;
-    }
-  } else {
-    for (int e = c; e < E; e += gridDim.x) {
-      int32_t* col = slice_hist + size_t(e) * gridDim.x;
-      for (int i = tid; i < int(gridDim.x); i += kFusedThreads) rows_s[i] = __ldcg(col + i);
-      __syncthreads();
-      const int total = block_exclusive_scan(rows_s, gridDim.x);
-      for (int i = tid; i < int(gridDim.x); i += kFusedThreads) col[i] = rows_s[i];
-      if (tid == 0) counts[e] = total;
-      __syncthreads();
-    }
-    grid_barrier(bar_count, bar_gen, status);
-    for (int e = tid; e < E; e += kFusedThreads) {
-      h[e] = __ldcg(slice_hist + size_t(e) * gridDim.x + c);
-      tot[e] = __ldcg(counts + e);
     }
   }
   __syncthreads();
@@ -917,9 +966,11 @@ static int launch_permute_fused(const moe_cfg& c, const void* x, const int32_t* 
   int* status = ws_ptr<int>(ws, L.status);
   unsigned int* bar_count = ws_ptr<unsigned int>(ws, L.bar_count);
   unsigned int* bar_gen = ws_ptr<unsigned int>(ws, L.bar_gen);
+  unsigned int* seq = ws_ptr<unsigned int>(ws, L.perm_seq);
+  int32_t* grp = ws_ptr<int32_t>(ws, L.grp_sums);
   void* args[] = {&idx_p, &x_p, &T, &E, &k, &T_loc, &n_ep, &cap, &tpc, &vec, &slice_hist,
                   &src_cnt, &counts, &offsets, &inv, &order, &xs, &status, &bar_count,
-                  &bar_gen};
+                  &bar_gen, &seq, &grp};
   const cudaError_t e = cudaLaunchCooperativeKernel(
       reinterpret_cast<const void*>(perm_fused_kernel), dim3(grid), dim3(kFusedThreads), args,
       0, st);
@@ -992,7 +1043,10 @@ int launch_ep_layout(const moe_cfg& c, const int32_t* idx, const int32_t* offset
   const bool fp8 = x && send_fp8 && send_scale;
   const bool rows = fp8 || (x && send_buf);
   // assignments per CTA: whole tokens; when rows move, one token per warp (as
-  // many rows in flight as a plain scatter), else up to kEpMaxPerCta
+  // many rows in flight as a plain scatter), else up to kEpMaxPerCta.  (A grid
+  // of the CTAs that fit at once, each taking more tokens, measured slower:
+  // the skewed layer 41 against 37.5 us, DS-V3 211 against 197 us; with
+  // several waves one CTA's tables overlap another's row moves.)
   int tok_per_cta = rows ? kPermThreads / 32 : kEpMaxPerCta / c.k;
   if (tok_per_cta < 1) tok_per_cta = 1;
   const int apc = tok_per_cta * c.k;

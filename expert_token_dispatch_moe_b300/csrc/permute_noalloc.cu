@@ -91,8 +91,9 @@ MOE_API int moe_permute_noalloc(const moe_cfg* c, const moe_bf16* x, const int32
   void* ws = scratch_address(dev, &err);
   if (!ws) return err;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the status word and the histogram's finished-CTA counter must start at zero
-  // (the per-(rank, expert) counts are cleared by the permute)
-  if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) return MOE_E_CUDA;
+  // the status word, the histogram's finished-CTA counter and the one-launch
+  // permute's group sums must start at zero (the per-(rank, expert) counts are
+  // cleared by the permute)
+  if (cudaMemsetAsync(ws, 0, kWsHeadBytes, st) != cudaSuccess) return MOE_E_CUDA;
   return launch_permute(*c, x, topk_idx, counts, offsets, order, inv, x_sorted, ws, st);
 }

@@ -90,8 +90,11 @@ int64_t moe_grouped_rows(const moe_cfg* cfg);
  * invalid configuration).  Host only. */
 size_t moe_workspace_bytes(const moe_cfg* cfg);
 
-/* Zero the workspace's device status word.  Call once after allocating the
- * workspace.  ws_bytes is the size of the caller's workspace allocation; every
+/* Zero the workspace's header: the device status word, the counters of the
+ * permute's grid barrier and the one-launch permute's per-group sums (the
+ * first 16,640 bytes, at fixed offsets for every configuration; the calls keep
+ * them consistent from then on).  Call once after allocating the workspace.
+ * ws_bytes is the size of the caller's workspace allocation; every
  * call taking a workspace returns MOE_E_WORKSPACE when ws is NULL or ws_bytes <
  * moe_workspace_bytes(cfg). */
 int moe_workspace_init(const moe_cfg* cfg, void* ws, size_t ws_bytes, void* stream);

@@ -173,6 +173,33 @@ def test_permute_one_launch_parity(m, name):
         _check_permute(cfg, x_dev, idx_np, out, lay)
 
 
+def test_permute_one_launch_shared_workspace(m):
+    """One workspace for one-launch permutes of several shapes, back to back.  The
+    per-group slice counts alternate between two buffers (each call clears the
+    other one), so every call must find its buffer zero whatever ran before."""
+    names = ["e48_k3", "e16_cap", "e8_ragged", "e64_k8", "e48_k3", "e64_k8", "e16_cap", "e1"]
+    cfgs = [ONE_LAUNCH[n] for n in names]
+    ws_bytes = max(m.moe_workspace_bytes(m.MoeCfg.from_layer(cfg)) for cfg in cfgs)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    m.moe_workspace_init(m.MoeCfg.from_layer(cfgs[0]), ws)
+    i32 = torch.int32
+    for i, cfg in enumerate(cfgs):
+        c = m.MoeCfg.from_layer(cfg)
+        scores = synth.make_scores(cfg, seed=40 + i)
+        idx_np = oracle.select_experts(scores.numpy(), cfg.k)
+        counts = torch.empty(cfg.E, dtype=i32, device="cuda")
+        offsets = torch.empty(cfg.E + 1, dtype=i32, device="cuda")
+        order = torch.empty(cfg.R, dtype=i32, device="cuda")
+        inv = torch.empty(cfg.A, dtype=i32, device="cuda")
+        idx = torch.from_numpy(idx_np.astype(np.int32)).cuda()
+        m.moe_permute(c, None, idx, counts, offsets, order, inv, None, ws)
+        torch.cuda.synchronize()
+        ref = oracle.permute(idx_np, cfg.E, cfg.capacity)
+        for key, t in (("counts", counts), ("offsets", offsets), ("order", order), ("inv", inv)):
+            assert np.array_equal(npi(t), ref[key]), (names[i], i, key)
+    assert m.moe_get_device_status(ws) == 0
+
+
 def test_permute_one_launch_indices_only(m):
     cfg = ONE_LAUNCH["e16_cap"]
     scores = synth.make_scores(cfg, seed=33)
