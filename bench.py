@@ -407,29 +407,39 @@ def _ffn_bytes(cfg, counts_np):
     return w + rows * cfg.d * 2 * 2 + rows * cfg.f * 2 * 2
 
 
-PEAK_RULE = ("burst bf16 peak, unless sw_power_cap was active in more than half of the clock "
-             "samples of the timed region: then the sustained (power-capped) bf16 peak")
+PEAK_RULE = ("burst bf16 peak, unless the timed region lasted at least 1 s with sw_power_cap "
+             "active in more than half of its clock samples and the median SM clock below the "
+             "maximum: then the sustained (power-capped) bf16 peak")
 
 
-def _tensor_peak(pk, clocks):
-    """The bf16 denominator for a kernel timed in this run, by PEAK_RULE."""
-    capped = bool(clocks) and clocks.get("power_cap_share", 0.0) > 0.5
+def _tensor_peak(pk, clocks, timed_s):
+    """The bf16 denominator for a kernel timed in this run, by PEAK_RULE: the
+    sustained peak was measured over seconds of back-to-back GEMMs at the
+    power limit, so it applies only to a timed region that long that also ran
+    capped and below the top clock."""
+    c = clocks or {}
+    capped = (timed_s >= 1.0 and c.get("power_cap_share", 0.0) > 0.5
+              and c.get("sm_mhz") is not None and c.get("sm_max_mhz") is not None
+              and c["sm_mhz"] < c["sm_max_mhz"])
     if capped and pk["bf16_tflops_sustained"]:
         return pk["bf16_tflops_sustained"], pk["source"] + " sustained"
     return pk["bf16_tflops"], pk["source"] + " burst"
 
 
-def _roofline(cfg, ffn_ms, ffn_flops, ffn_bytes, pk, clocks):
+def _roofline(cfg, ffn_ms, ffn_flops, ffn_bytes, pk, clocks, timed_s):
     """The dominant kernel (both grouped GEMM launches of a step) against the
     roofline that bounds it: the bf16 peak when its FLOPs take longer than its
     bytes at the measured copy bandwidth, else HBM.  The bf16 denominator
     follows PEAK_RULE from this run's own clock samples; both fractions are
     reported."""
-    peak_tf, src = _tensor_peak(pk, clocks)
+    peak_tf, src = _tensor_peak(pk, clocks, timed_s)
     t_flops = ffn_flops / (peak_tf * 1e12)
     t_bytes = ffn_bytes / (pk["hbm_gbs"] * 1e9)
     tflops = ffn_flops / (ffn_ms * 1e-3) / 1e12
-    base = {"kernel": "grouped_gemm_kernel (GEMM 1 + GEMM 2 of one step)",
+    import expert_token_dispatch_moe_b300 as m
+    kname = "grouped_pair_kernel" if m.moe_ffn_pair_tiles(m.MoeCfg.from_layer(cfg)) \
+        else "grouped_gemm_kernel"
+    base = {"kernel": f"{kname} (GEMM 1 + GEMM 2 of one step)",
             "traffic": _profiled_traffic(cfg), "algorithmic_bytes": ffn_bytes,
             "algorithmic_flops": ffn_flops}
     if t_flops >= t_bytes:
@@ -612,7 +622,7 @@ def run_ours(args, cfg):
                                   "layer, copy out), L2 flushed between steps"}},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": _roofline(cfg, kt["grouped_ffn"], alg["ffn_flops"], _ffn_bytes(cfg, counts),
-                              pk, clk),
+                              pk, clk, wall),
         "kernels": kernels,
         "layout": layout_metrics(cfg, counts, layer.count_mat.cpu().numpy()),
         "wall_s": wall,

@@ -31,7 +31,7 @@ ERRORS = {
 EXPORTS = ("moe_validate_cfg", "moe_grouped_rows", "moe_workspace_bytes", "moe_workspace_init",
            "moe_pack_router", "moe_router_logits", "moe_route", "moe_permute", "moe_permute_noalloc",
            "moe_ep_layout", "moe_ep_layout_fp8", "moe_dispatch_recv_fp8", "moe_pack_w13",
-           "moe_grouped_ffn", "moe_grouped_ffn_gather", "moe_grouped_ffn_train", "moe_combine", "moe_bias_update", "moe_eplb_plan",
+           "moe_grouped_ffn", "moe_ffn_pair_tiles", "moe_grouped_ffn_gather", "moe_grouped_ffn_train", "moe_combine", "moe_bias_update", "moe_eplb_plan",
            "moe_eplb_dispatch", "moe_pack_backward", "moe_combine_backward",
            "moe_backward_workspace_bytes", "moe_grouped_ffn_backward", "moe_permute_backward",
            "moe_selftest_wait_timeout", "moe_get_device_status", "moe_strerror",
@@ -110,6 +110,7 @@ _sig = {
     "moe_dispatch_recv_fp8": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
     "moe_pack_w13": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
     "moe_grouped_ffn": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_ffn_pair_tiles": (ctypes.c_int, [_CFG]),
     "moe_grouped_ffn_gather": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                               _P]),
     "moe_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
@@ -174,6 +175,13 @@ def moe_validate_cfg(cfg: MoeCfg) -> int:
 
 def moe_grouped_rows(cfg: MoeCfg) -> int:
     return _lib.moe_grouped_rows(ctypes.byref(cfg))
+
+
+def moe_ffn_pair_tiles(cfg: MoeCfg) -> bool:
+    """True when moe_grouped_ffn takes SM-pair tiles for cfg (MOE_FFN_TILES read now)."""
+    rc = _lib.moe_ffn_pair_tiles(ctypes.byref(cfg))
+    _check(min(rc, 0), "moe_ffn_pair_tiles")
+    return rc == 1
 
 
 def moe_workspace_bytes(cfg: MoeCfg) -> int:

@@ -824,7 +824,7 @@ int launch_pack_router(const moe_cfg& c, const float* W, void* out, cudaStream_t
 // reach 768.  The environment variable MOE_FFN_TILES = "pair" or "single"
 // overrides the choice (read at every call).  The gathered and training forms
 // always take the one-SM tiles.
-static bool use_pair_tiles(const moe_cfg& c) {
+bool use_pair_tiles(const moe_cfg& c) {
   const char* v = getenv("MOE_FFN_TILES");
   if (v && strcmp(v, "pair") == 0) return true;
   if (v && strcmp(v, "single") == 0) return false;

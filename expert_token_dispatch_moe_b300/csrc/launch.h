@@ -72,6 +72,10 @@ int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
                        const void* W13, const void* W2, void* h, void* y_sorted, void* g1,
                        void* ws, cudaStream_t st);
 // The forward FFN on SM pairs (two-CTA clusters, transposed tiles).
+// The grouped FFN's choice of SM-pair tiles for this configuration (the shape
+// rule, or MOE_FFN_TILES when set).
+bool use_pair_tiles(const moe_cfg& c);
+
 int launch_grouped_ffn_pair(const moe_cfg& c, const void* x_sorted, const void* x,
                             const int32_t* counts, const int32_t* offsets, const void* W13,
                             const void* W2, void* h, void* y_sorted, int* status,

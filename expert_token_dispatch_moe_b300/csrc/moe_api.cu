@@ -234,6 +234,11 @@ MOE_API int moe_pack_w13(const moe_cfg* c, const moe_bf16* W1, const moe_bf16* W
   return launch_pack_w13(*c, W1, W3, W13, static_cast<cudaStream_t>(stream));
 }
 
+MOE_API int moe_ffn_pair_tiles(const moe_cfg* c) {
+  MOE_TRY(moe_validate_cfg(c));
+  return use_pair_tiles(*c) ? 1 : 0;
+}
+
 MOE_API int moe_grouped_ffn(const moe_cfg* c, const moe_bf16* x_sorted, const moe_bf16* x,
                             const int32_t* counts, const int32_t* offsets, const moe_bf16* W13,
                             const moe_bf16* W2, moe_bf16* h, moe_bf16* y_sorted, void* ws,

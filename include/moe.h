@@ -280,6 +280,12 @@ int moe_grouped_ffn(const moe_cfg* cfg, const moe_bf16* x_sorted, const moe_bf16
                     const moe_bf16* W13, const moe_bf16* W2, moe_bf16* h,
                     moe_bf16* y_sorted, void* ws, size_t ws_bytes, void* stream);
 
+/* The tiles moe_grouped_ffn takes for this configuration now (the rule above,
+ * MOE_FFN_TILES read at this call): 1 for SM pairs (grouped_pair_kernel), 0 for
+ * one-SM tiles (grouped_gemm_kernel), or a negative error code for an invalid
+ * configuration.  Host only; no device is touched. */
+int moe_ffn_pair_tiles(const moe_cfg* cfg);
+
 /* moe_grouped_ffn with the permute's row move fused into GEMM 1's operand
  * loads ("Token permutation and grouped GEMMs": production kernels fuse the
  * permutation into the grouped GEMM's loads, saving a full read and write of

@@ -163,3 +163,25 @@ def test_workspace_holds_router_k_split_partials(m):
         assert extra == (align(S * cfg.T * cfg.E * 4) if S > 1 else 0), (name, kw, S)
     assert _k_split(128, 256, 7168) == 14 and _k_split(8192, 256, 7168) == 2
 
+
+
+def test_ffn_tile_choice(m, monkeypatch):
+    """moe_ffn_pair_tiles reports the grouped FFN's tiles: SM pairs from 768
+    expected rows per expert (capped by the capacity), one-SM tiles below, and
+    MOE_FFN_TILES overrides either way at the call."""
+    monkeypatch.delenv("MOE_FFN_TILES", raising=False)
+    pick = {n: m.moe_ffn_pair_tiles(m.MoeCfg.from_layer(synth.CONFIGS[n])) for n in synth.CONFIGS}
+    assert pick["mixtral"] is True          # 4096 * 2 / 8 = 1024 rows per expert
+    assert pick["dsv3"] is False and pick["dsv3_decode"] is False and pick["tiny"] is False
+    assert pick["skew"] is False            # 512 rows per expert, capacity 640
+    edge = synth.CONFIGS["tiny"].with_(T=3072, E=8, k=2)   # exactly 768
+    assert m.moe_ffn_pair_tiles(m.MoeCfg.from_layer(edge)) is True
+    assert m.moe_ffn_pair_tiles(m.MoeCfg.from_layer(edge.with_(T=3064))) is False
+    capped = synth.CONFIGS["mixtral"].with_(capacity=700)
+    assert m.moe_ffn_pair_tiles(m.MoeCfg.from_layer(capped)) is False
+    monkeypatch.setenv("MOE_FFN_TILES", "single")
+    assert m.moe_ffn_pair_tiles(m.MoeCfg.from_layer(synth.CONFIGS["mixtral"])) is False
+    monkeypatch.setenv("MOE_FFN_TILES", "pair")
+    assert m.moe_ffn_pair_tiles(m.MoeCfg.from_layer(synth.CONFIGS["tiny"])) is True
+    with pytest.raises(m.MoeError):
+        m.moe_ffn_pair_tiles(m.MoeCfg.from_layer(synth.CONFIGS["tiny"].with_(k=0)))

@@ -49,3 +49,22 @@ def test_layout_metrics_eta_matches_the_oracle():
         assert got["eta"] == oracle.imbalance_eta(C)
     # tiles: 300 rows -> 128 + 128 + a 64-row half tile; 200 -> 128 + 128; 0 -> nothing
     assert b.tile_rows([300, 200, 0, 64, 65]) == 320 + 256 + 0 + 64 + 128
+
+
+def test_tensor_peak_rule():
+    """The sustained bf16 peak (seconds of back-to-back GEMMs at the power limit)
+    is the denominator only for a timed region that long which also ran capped
+    below the top clock; otherwise the burst peak."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    pk = {"bf16_tflops": 1749.0, "bf16_tflops_sustained": 1350.5, "source": "measured"}
+    capped_low = {"power_cap_share": 0.9, "sm_mhz": 1500.0, "sm_max_mhz": 2032.0}
+    capped_top = {"power_cap_share": 0.9, "sm_mhz": 2032.0, "sm_max_mhz": 2032.0}
+    assert b._tensor_peak(pk, capped_low, 2.5)[0] == 1350.5
+    assert b._tensor_peak(pk, capped_low, 0.05)[0] == 1749.0   # a short region: burst
+    assert b._tensor_peak(pk, capped_top, 2.5)[0] == 1749.0    # capped but at the top clock
+    assert b._tensor_peak(pk, {"power_cap_share": 0.2, "sm_mhz": 1500.0,
+                               "sm_max_mhz": 2032.0}, 2.5)[0] == 1749.0
+    assert b._tensor_peak(pk, None, 5.0)[0] == 1749.0
