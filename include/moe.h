@@ -224,14 +224,16 @@ int moe_dispatch_recv_fp8(const moe_cfg* cfg, const uint8_t* send_fp8, const flo
  * Outputs, arguments and results are those of moe_permute.  The scratch lives in
  * a fixed 1 MiB array in device memory that the library holds on every GPU that
  * loads it, until the process exits.
- *  - A configuration whose permute scratch (status word, per-(rank, expert)
- *    counts and per-2048-assignment histograms) exceeds 1 MiB is rejected on the
- *    host with MOE_E_SCRATCH_LIMIT.
+ *  - A configuration whose permute scratch (the workspace header: status word,
+ *    counters, the one-launch permute's barrier words and group sums; then the
+ *    per-(rank, expert) counts, per-2048-assignment histograms and, with E <= 64,
+ *    per-CTA slice histograms) exceeds 1 MiB is rejected on the host with
+ *    MOE_E_SCRATCH_LIMIT.
  *  - The first call on a device looks up the array's device address.  Make that
  *    first call before any stream capture on that device.
  *  - Every call shares the one array.  Calls that overlap on the GPU (on
  *    different streams, or from host threads without ordering) race on it.
- *  - Each call clears the status word and counters it uses.  Bad expert ids are
+ *  - Each call clears the workspace header (status word, counters, group sums).  Bad expert ids are
  *    treated as dropped (inv = -1) as in moe_permute, but the status word is not
  *    readable from outside: such ids are dropped silently.
  *  - The per-(source rank, expert) histogram stays in the hidden array, so
