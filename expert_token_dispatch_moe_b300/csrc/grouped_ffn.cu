@@ -56,7 +56,7 @@ struct GroupedParams {
   int E, capacity, has_shared, T, R;
   int dense_rows;
   int K;                  // reduction length of one pass
-  int k_passes;           // passes over K: A re-read each pass, B advanced by b_pass_rows
+  int k_passes;           // passes over K (interleaved per k-block), B advanced by b_pass_rows
   int b_pass_rows;
   int k_split;            // dense mode: > 1 = segment g reduces K chunk g (length K) into
                           //   its own partial output rows [g*dense_rows, (g+1)*dense_rows)
@@ -173,6 +173,9 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
   const bool wgrad = p.kpad_off != nullptr;
   const int kb_per_pass = wgrad ? (1 << 30) : p.K / BK;
   const int n_b = kMerge ? p.k_passes : 1;  // B boxes per stage
+  // passes over K taken k-block by k-block (pass = kb % n_pass): the passes'
+  // B boxes of one k-block follow each other, so A's box is re-read from L2
+  const int n_pass = kMerge || wgrad ? 1 : p.k_passes;
   const int num_kb = wgrad ? 0 : (kMerge ? kb_per_pass : kb_per_pass * p.k_passes);
   // first column and k-blocks of segment g's reduction
   auto tile_k = [&](int g, int& k0, int& nkb) {
@@ -292,8 +295,8 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
           for (int kb = 0; kb < nkb; ++kb) {
             if (!wait_or_abort(&ctl.empty[stage], phase ^ 1u, ctl, p.status)) { ok = false; break; }
             uint8_t* sa = smem + stage * STAGE_BYTES;
-            const int pass = kb / kb_per_pass;
-            const int ka = k0 + (kb - pass * kb_per_pass) * BK;
+            const int pass = kb % n_pass;
+            const int ka = k0 + (kb / n_pass) * BK;
             mbar_arrive_expect_tx(&ctl.full[stage], tx);
             tma_load_2d(sa, ma, ka, a_row, &ctl.full[stage]);
             if (!kMerge) {
@@ -336,8 +339,8 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!ok) break;
           uint8_t* sa = smem + stage * STAGE_BYTES;
-          const int pass = kb / kb_per_pass;
-          const int ka = (kb - pass * kb_per_pass) * BK;
+          const int pass = kb % n_pass;
+          const int ka = (kb / n_pass) * BK;
           if (lane == 0) mbar_arrive_expect_tx(&ctl.full[stage], tx);
           __syncwarp();
           if (gather) {
