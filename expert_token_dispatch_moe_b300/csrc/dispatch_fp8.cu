@@ -43,9 +43,12 @@ __global__ void __launch_bounds__(256) fp8_recv_kernel(const uint4* __restrict__
     const uint4* src = send_fp8 + size_t(p) * vec16_per_row;  // 16 codes per vector
     uint4* dst = x_sorted + size_t(row) * 2 * vec16_per_row;   // 8 bf16 per vector
     // eight code vectors in flight per lane (a row of up to 4096 elements at
-    // once), then their conversions.  (Items of 512 codes strided over all
-    // warps, four in flight, measured slower: 0.48 against 0.50 of the copy
-    // peak on the Mixtral shape, 0.66 against 0.75 on the skewed layer.)
+    // once), then their conversions.  Two other arrangements measured no
+    // better: items of 512 codes strided over all warps, four in flight (0.48
+    // against 0.50 of the copy peak on the Mixtral shape, 0.66 against 0.75 on
+    // the skewed layer); and a one-wave grid whose warps resolve 32 slots'
+    // indices at once and stream their rows through two register buffers
+    // (Mixtral shape 28.5 against 27.4 us, DS-V3 284 against 297 us).
     constexpr int U = 8;
     for (int v0 = lane; v0 < vec16_per_row; v0 += 32 * U) {
       uint4 c[U];
