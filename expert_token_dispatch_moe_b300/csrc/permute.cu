@@ -6,7 +6,7 @@
 // rank of an assignment inside its expert comes from histograms and prefix
 // sums, never from the order of atomics, so every output is deterministic.
 // Three paths: up to 4096 assignments (and 256 experts), one CTA computes the
-// indices; up to 64 experts, one cooperative launch does everything
+// indices; up to 256 experts, one cooperative launch does everything
 // (perm_fused_kernel, below); otherwise:
 //   1. hist:  per 2048-assignment chunk, a histogram over experts (shared-memory
 //             atomics: only counts, not order, depend on them); counts per
@@ -748,27 +748,36 @@ __global__ void __launch_bounds__(kFusedThreads) perm_fused_kernel(
         }
       }
     } else {
+      // 16-byte words of the expert's rows: kG4 of group sums (word j holds
+      // groups 4j..4j+3), then kS4 of its group's slice counts (CTAs c_first +
+      // 4j'..); the P threads of the expert take words p, p + P, ...
       const int nq = (int(gridDim.x) + kFusedGroupCtas - 1) / kFusedGroupCtas;
       const int c_first = q * kFusedGroupCtas;
-      const int n_words = nq + (c - c_first);
-      constexpr int kMaxWords = (kFusedMaxGroups + kFusedGroupCtas + 3) / 4;  // P >= 4
-      int v[kMaxWords];
+      constexpr int kG4 = kFusedMaxGroups / 4, kS4 = kFusedGroupCtas / 4;
+      constexpr int kW4 = kG4 + kS4;
+      int4 v[kW4];
       if (e < E) {
-        const int32_t* gs = gsum + e * kFusedMaxGroups;
-        const int32_t* hs = slice_hist + e * kFusedMaxCtas;
+        const int4* gs = reinterpret_cast<const int4*>(gsum + e * kFusedMaxGroups);
+        const int4* hs = reinterpret_cast<const int4*>(slice_hist + e * kFusedMaxCtas + c_first);
 #pragma unroll
-        for (int i = 0; i < kMaxWords; ++i) {
+        for (int i = 0; i < kW4; ++i) {
           const int j = p + i * P;
-          v[i] = j < nq ? __ldcg(gs + j) : (j < n_words ? __ldcg(hs + (c_first + j - nq)) : 0);
+          const bool load = j < kG4 ? 4 * j < nq : (j < kW4 && c_first + 4 * (j - kG4) < c);
+          v[i] = load ? __ldcg(j < kG4 ? gs + j : hs + (j - kG4)) : make_int4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int i = 0; i < kMaxWords; ++i) {
+        for (int i = 0; i < kW4; ++i) {
           const int j = p + i * P;
-          if (j < nq) {
-            total += v[i];
-            if (j < q) before += v[i];
-          } else {
-            before += v[i];
+          const int x4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (j < kG4) {
+              const int gq = 4 * j + u;  // group
+              if (gq < nq) total += x4[u];
+              if (gq < q) before += x4[u];
+            } else if (j < kW4) {
+              if (c_first + 4 * (j - kG4) + u < c) before += x4[u];
+            }
           }
         }
       }
@@ -785,17 +794,29 @@ __global__ void __launch_bounds__(kFusedThreads) perm_fused_kernel(
   }
   __syncthreads();
   if (warp == 0) {
-    const int e0 = 2 * lane;
-    const int v0 = e0 < E ? tot[e0] : 0, v1 = e0 + 1 < E ? tot[e0 + 1] : 0;
-    int incl = v0 + v1;
+    // lane L scans experts kPer*L .. kPer*L + kPer - 1
+    constexpr int kPer = kFusedMaxE / 32;
+    int loc[kPer];
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane * kPer + i;
+      loc[i] = e < E ? tot[e] : 0;
+      sum += loc[i];
+    }
+    int incl = sum;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int o = __shfl_up_sync(0xffffffffu, incl, off);
       if (lane >= off) incl += o;
     }
-    const int excl = incl - v0 - v1;
-    if (e0 < E) seg[e0] = excl;
-    if (e0 + 1 < E) seg[e0 + 1] = excl + v0;
+    int run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane * kPer + i;
+      if (e < E) seg[e] = run;
+      run += loc[i];
+    }
     if (lane == 31) seg[E] = incl;
   }
   __syncthreads();

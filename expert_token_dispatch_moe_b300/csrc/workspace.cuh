@@ -31,7 +31,7 @@ namespace moe {
 //                                    splits K into S > 1 chunks (router_k_split)
 // ---------------------------------------------------------------------------
 constexpr int kPermChunk = 2048;   // assignments per histogram/rank CTA
-constexpr int kFusedMaxE = 64;     // the one-launch permute's largest expert count
+constexpr int kFusedMaxE = 256;    // the one-launch permute's largest expert count
 constexpr int kFusedMaxCtas = 512; // and its most CTAs
 constexpr int kFusedGroupCtas = 16; // CTAs per group of its slice-count sums
 constexpr int kFusedMaxGroups = kFusedMaxCtas / kFusedGroupCtas;

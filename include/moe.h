@@ -92,7 +92,7 @@ size_t moe_workspace_bytes(const moe_cfg* cfg);
 
 /* Zero the workspace's header: the device status word, the counters of the
  * permute's grid barrier and the one-launch permute's per-group sums (the
- * first 16,640 bytes, at fixed offsets for every configuration; the calls keep
+ * first 65,792 bytes, at fixed offsets for every configuration; the calls keep
  * them consistent from then on).  Call once after allocating the workspace.
  * ws_bytes is the size of the caller's workspace allocation; every
  * call taking a workspace returns MOE_E_WORKSPACE when ws is NULL or ws_bytes <
@@ -226,7 +226,7 @@ int moe_dispatch_recv_fp8(const moe_cfg* cfg, const uint8_t* send_fp8, const flo
  * loads it, until the process exits.
  *  - A configuration whose permute scratch (the workspace header: status word,
  *    counters, the one-launch permute's barrier words and group sums; then the
- *    per-(rank, expert) counts, per-2048-assignment histograms and, with E <= 64,
+ *    per-(rank, expert) counts, per-2048-assignment histograms and, with E <= 256,
  *    per-CTA slice histograms) exceeds 1 MiB is rejected on the host with
  *    MOE_E_SCRATCH_LIMIT.
  *  - The first call on a device looks up the array's device address.  Make that

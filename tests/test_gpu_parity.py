@@ -158,6 +158,9 @@ ONE_LAUNCH = {
     "e64_k8": C["tiny"].with_(name="e64_k8", T=4104, E=64, k=8, n_ep=8, d=64),
     "e16_cap": C["tiny"].with_(name="e16_cap", T=6000, E=16, k=2, n_ep=4, d=192, capacity=600),
     "e1": C["tiny"].with_(name="e1", T=5000, E=1, k=1, n_ep=1, d=64),
+    "e128_k4": C["tiny"].with_(name="e128_k4", T=3000, E=128, k=4, n_ep=8, d=128),
+    "e256_k8": C["tiny"].with_(name="e256_k8", T=4096, E=256, k=8, n_ep=64, d=64),
+    "e256_cap": C["tiny"].with_(name="e256_cap", T=5008, E=256, k=4, n_ep=16, d=64, capacity=70),
     "fallback": C["tiny"].with_(name="fallback", T=80000, E=8, k=8, n_ep=8, d=64),
 }
 
@@ -177,7 +180,8 @@ def test_permute_one_launch_shared_workspace(m):
     """One workspace for one-launch permutes of several shapes, back to back.  The
     per-group slice counts alternate between two buffers (each call clears the
     other one), so every call must find its buffer zero whatever ran before."""
-    names = ["e48_k3", "e16_cap", "e8_ragged", "e64_k8", "e48_k3", "e64_k8", "e16_cap", "e1"]
+    names = ["e48_k3", "e16_cap", "e256_k8", "e8_ragged", "e64_k8", "e128_k4", "e48_k3", "e256_cap",
+             "e64_k8", "e16_cap", "e1"]
     cfgs = [ONE_LAUNCH[n] for n in names]
     ws_bytes = max(m.moe_workspace_bytes(m.MoeCfg.from_layer(cfg)) for cfg in cfgs)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
