@@ -460,7 +460,9 @@ def _roofline(cfg, ffn_ms, ffn_flops, ffn_bytes, pk, clocks, timed_s):
         gbs = ffn_bytes / (ffn_ms * 1e-3) / 1e9
         base.update({"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": gbs / pk["hbm_gbs"], "peak_source": pk["source"] + " copy",
-                     "tflops": tflops})
+                     "tflops": tflops, "frac_of_burst_peak": tflops / pk["bf16_tflops"],
+                     "frac_of_sustained_peak": (tflops / pk["bf16_tflops_sustained"]
+                                                if pk["bf16_tflops_sustained"] else None)})
     return base
 
 
