@@ -285,10 +285,35 @@ def _time_extras(m, layer, c, cfg, x, st, flush, counts, pk, reps):
     out = _time_fp8_and_balance(m, layer, c, cfg, x, st, flush, counts, pk, reps, timed, out,
                                 send_fp8)
     del send_fp8
+    if not layer.gather:
+        out.update(_time_combine_epilogue(m, layer, c, cfg, x, counts, timed))
     # backward of the layer (routing fixed), on the forward's buffers
     if not layer.gather:
         out.update(_time_backward(m, layer, c, cfg, x, st, flush, counts, pk, reps))
     return out
+
+
+def _time_combine_epilogue(m, layer, c, cfg, x, counts, timed):
+    """The grouped FFN with the combine in GEMM 2's epilogue (bf16 reductions
+    into y, no y_sorted) against the two calls it replaces, each timed alone
+    the same way."""
+    xs = x if cfg.has_shared else None
+    y_f = torch.empty_like(layer.y)
+    fused = timed(lambda: m.moe_grouped_ffn_combine(c, layer.x_sorted, xs, layer.counts,
+                                                    layer.offsets, layer.W13, layer.W2, layer.h,
+                                                    layer.order, layer.topk_gate, y_f, layer.ws))
+
+    def unfused():
+        m.moe_grouped_ffn(c, layer.x_sorted, xs, layer.counts, layer.offsets, layer.W13,
+                          layer.W2, layer.h, layer.y_sorted, layer.ws)
+        m.moe_combine(c, layer.y_sorted, layer.inv, layer.topk_gate, layer.y)
+    pair = timed(unfused)
+    kept = int(np.minimum(counts, cfg.capacity).sum()) if cfg.capacity else cfg.A
+    rows = kept + (cfg.T if cfg.has_shared else 0)
+    flops = 6.0 * cfg.d * cfg.f * rows
+    return {"ffn_combine_fused": {"ms": fused, "tflops": flops / (fused * 1e-3) / 1e12,
+                                  "unfused_ffn_then_combine_ms": pair,
+                                  "tiles": "one-SM (the epilogue exists there only)"}}
 
 
 def _time_backward(m, layer, c, cfg, x, st, flush, counts, pk, reps):

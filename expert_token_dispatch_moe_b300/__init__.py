@@ -31,7 +31,7 @@ ERRORS = {
 EXPORTS = ("moe_validate_cfg", "moe_grouped_rows", "moe_workspace_bytes", "moe_workspace_init",
            "moe_pack_router", "moe_router_logits", "moe_route", "moe_permute", "moe_permute_noalloc",
            "moe_ep_layout", "moe_ep_layout_fp8", "moe_dispatch_recv_fp8", "moe_pack_w13",
-           "moe_grouped_ffn", "moe_ffn_pair_tiles", "moe_grouped_ffn_gather", "moe_grouped_ffn_train", "moe_combine", "moe_bias_update", "moe_eplb_plan",
+           "moe_grouped_ffn", "moe_ffn_pair_tiles", "moe_grouped_ffn_combine", "moe_grouped_ffn_gather", "moe_grouped_ffn_train", "moe_combine", "moe_bias_update", "moe_eplb_plan",
            "moe_eplb_dispatch", "moe_pack_backward", "moe_combine_backward",
            "moe_backward_workspace_bytes", "moe_grouped_ffn_backward", "moe_permute_backward",
            "moe_selftest_wait_timeout", "moe_get_device_status", "moe_strerror",
@@ -111,6 +111,8 @@ _sig = {
     "moe_pack_w13": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
     "moe_grouped_ffn": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_ffn_pair_tiles": (ctypes.c_int, [_CFG]),
+    "moe_grouped_ffn_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                               _SZ, _P]),
     "moe_grouped_ffn_gather": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                               _P]),
     "moe_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
@@ -266,6 +268,15 @@ def moe_grouped_ffn_gather(cfg, x, order, counts, offsets, W13, W2, h, y_sorted,
                                        _ptr(offsets), _ptr(W13), _ptr(W2), _ptr(h),
                                        _ptr(y_sorted), p, n, _stream(stream)),
            "moe_grouped_ffn_gather")
+
+
+def moe_grouped_ffn_combine(cfg, x_sorted, x, counts, offsets, W13, W2, h, order, topk_gate, y, ws,
+                            stream=None):
+    p, n = _ws(ws)
+    _check(_lib.moe_grouped_ffn_combine(ctypes.byref(cfg), _ptr(x_sorted), _ptr(x), _ptr(counts),
+                                        _ptr(offsets), _ptr(W13), _ptr(W2), _ptr(h), _ptr(order),
+                                        _ptr(topk_gate), _ptr(y), p, n, _stream(stream)),
+           "moe_grouped_ffn_combine")
 
 
 def moe_combine(cfg, y_sorted, inv, topk_gate, y, stream=None):

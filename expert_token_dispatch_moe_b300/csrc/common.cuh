@@ -15,6 +15,14 @@
 
 namespace moe {
 
+// y[0..7] += v (eight bf16 as four bf16x2 words), one 16-byte reduction in L2
+// (each element rounded to bf16 after its add).  addr 16-byte aligned.
+__device__ __forceinline__ void red_add_bf16x8(void* addr, const uint32_t (&v)[4]) {
+  asm volatile("red.global.add.noftz.v4.bf16x2 [%0], {%1, %2, %3, %4};" ::"l"(addr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3])
+               : "memory");
+}
+
 // Record the first device-side error in the workspace status word.
 __device__ __forceinline__ void report_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);

@@ -48,7 +48,7 @@ constexpr uint32_t EPI_STAGE_BYTES = 32 * 128;  // per epilogue warp: 32 rows x 
 constexpr size_t DYN_SMEM = size_t(STAGES) * STAGE_BYTES + 4 * EPI_STAGE_BYTES + 1024;
 }  // namespace gg
 
-enum { kEpiSwiglu = 0, kEpiBf16 = 1, kEpiF32 = 2, kEpiSwigluBwd = 3 };
+enum { kEpiSwiglu = 0, kEpiBf16 = 1, kEpiF32 = 2, kEpiSwigluBwd = 3, kEpiCombine = 4 };
 
 struct GroupedParams {
   const int32_t* counts;  // nullptr: one dense segment of dense_rows rows at row 0
@@ -71,6 +71,9 @@ struct GroupedParams {
                           //   with u, v = aux[:, gate j], aux[:, up j] (packed like W13)
                           //   and s = sigmoid(u): out[:, gate j] = dh v s (1 + u (1 - s)),
                           //   out[:, up j] = dh u s
+                          // kEpiCombine: routed row r of assignment a = comb_order[r]
+                          //   adds bf16(comb_gate[a] * acc) into comb_y[a / comb_k]; the
+                          //   shared expert's row t adds bf16(acc) into comb_y[t]
   int shared_a_separate;  // 1: shared expert's A rows come from tmA_sh from row 0
   __nv_bfloat16* out;
   float* out_f32;
@@ -97,6 +100,12 @@ struct GroupedParams {
   // kEpiSwiglu: non-null = also keep the pre-activations, aux_out[:, n_blk*BN + c]
   // = bf16(acc[:, c]) (gate and up columns packed like W13), ld_aux
   __nv_bfloat16* aux_out;
+  // kEpiCombine: the assignment of each grouped row, the gates, top-k, and the
+  // token-order output (zeroed before the launch; row stride ld_out)
+  const int32_t* comb_order;
+  const float* comb_gate;
+  int comb_k;
+  __nv_bfloat16* comb_y;
 };
 
 struct GroupedCtl {
@@ -543,6 +552,42 @@ __global__ void __launch_bounds__(gg::THREADS, 1)
               dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
           }
         }
+      } else if (p.mode == kEpiCombine) {
+        // the row's token and gate: routed rows through the grouped order,
+        // the shared expert's rows are the tokens (gate 1)
+        int t = -1;
+        float gw = 1.0f;
+        if (valid) {
+          if (g < p.E) {
+            const int a = __ldg(p.comb_order + out_row0 + r);
+            if (a >= 0) {
+              t = a / p.comb_k;
+              gw = __ldg(p.comb_gate + a);
+            }
+          } else {
+            t = r;
+          }
+        }
+        const int col0 = n_blk * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(taddr + c, v);
+          tmem_ld_wait();
+          if (t >= 0) {
+            __nv_bfloat16* dst = p.comb_y + size_t(t) * p.ld_out + col0 + c;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              if (col0 + c + 8 * i >= p.N) break;
+              uint32_t w[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                w[q] = pack_bf16x2(gw * __uint_as_float(v[8 * i + 2 * q]),
+                                   gw * __uint_as_float(v[8 * i + 2 * q + 1]));
+              red_add_bf16x8(dst + 8 * i, w);
+            }
+          }
+        }
       } else if (p.tma_store && !half && m_blk * BM + quarter * 32 + 31 < rows) {
         // all 32 rows of this warp are valid: stage 64 columns at a time in
         // shared memory (128-byte swizzle) and store them with one tensor copy
@@ -836,14 +881,24 @@ bool use_pair_tiles(const moe_cfg& c) {
   return rows >= 768;
 }
 
-int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
-                       const int32_t* gather_order, const int32_t* counts, const int32_t* offsets,
-                       const void* W13, const void* W2, void* h, void* y_sorted, void* g1,
-                       void* ws, cudaStream_t st) {
+namespace {
+// GEMM 2 adding its rows straight into the token-order output (kEpiCombine)
+struct CombineOut {
+  const int32_t* order;
+  const float* gate;
+  void* y;
+};
+}  // namespace
+
+static int launch_grouped_ffn_impl(const moe_cfg& c, const void* x_sorted, const void* x,
+                                   const int32_t* gather_order, const int32_t* counts,
+                                   const int32_t* offsets, const void* W13, const void* W2,
+                                   void* h, void* y_sorted, void* g1, void* ws, cudaStream_t st,
+                                   const CombineOut* comb) {
   using namespace gg;
   if (!get_encoder()) return MOE_E_CUDA;
   const WsLayout L = ws_layout(c);
-  if (gather_order == nullptr && g1 == nullptr && use_pair_tiles(c))
+  if (gather_order == nullptr && g1 == nullptr && comb == nullptr && use_pair_tiles(c))
     return launch_grouped_ffn_pair(c, x_sorted, x, counts, offsets, W13, W2, h, y_sorted,
                                    ws_ptr<int>(ws, L.status), st);
   if (set_smem_attr() != MOE_OK) return MOE_E_CUDA;
@@ -913,12 +968,42 @@ int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
   p2.ld_out = c.d;
   const long long t2 = mt_ub * ((p2.N + BN - 1) / BN);
   const int grid2 = int(t2 < sms ? t2 : sms);
-  CUtensorMap mOut2;
-  if (!make_bf16_map(&mOut2, y_sorted, rows_h, c.d, 32)) return MOE_E_CUDA;
-  p2.tma_store = 1;
+  CUtensorMap mOut2 = mB2;  // unused without the tensor-store epilogue
+  if (comb) {
+    p2.mode = kEpiCombine;
+    p2.out = nullptr;
+    p2.comb_order = comb->order;
+    p2.comb_gate = comb->gate;
+    p2.comb_k = c.k;
+    p2.comb_y = static_cast<__nv_bfloat16*>(comb->y);
+  } else {
+    if (!make_bf16_map(&mOut2, y_sorted, rows_h, c.d, 32)) return MOE_E_CUDA;
+    p2.tma_store = 1;
+  }
   grouped_gemm_kernel<false><<<grid2, THREADS, DYN_SMEM, st>>>(mA2, mA2, mA2h, mA2h, mB2, mOut2, p2);
   note_launches(2);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_E_CUDA;
+}
+
+int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
+                       const int32_t* gather_order, const int32_t* counts, const int32_t* offsets,
+                       const void* W13, const void* W2, void* h, void* y_sorted, void* g1,
+                       void* ws, cudaStream_t st) {
+  return launch_grouped_ffn_impl(c, x_sorted, x, gather_order, counts, offsets, W13, W2, h,
+                                 y_sorted, g1, ws, st, nullptr);
+}
+
+int launch_grouped_ffn_combine(const moe_cfg& c, const void* x_sorted, const void* x,
+                               const int32_t* counts, const int32_t* offsets, const void* W13,
+                               const void* W2, void* h, const int32_t* order, const float* gate,
+                               void* y, void* ws, cudaStream_t st) {
+  if (cudaMemsetAsync(y, 0, size_t(c.T) * c.d * 2, st) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_E_CUDA;
+  }
+  const CombineOut comb{order, gate, y};
+  return launch_grouped_ffn_impl(c, x_sorted, x, nullptr, counts, offsets, W13, W2, h, nullptr,
+                                 nullptr, ws, st, &comb);
 }
 
 }  // namespace moe

@@ -76,6 +76,13 @@ int launch_grouped_ffn(const moe_cfg& c, const void* x_sorted, const void* x,
 // rule, or MOE_FFN_TILES when set).
 bool use_pair_tiles(const moe_cfg& c);
 
+// The grouped FFN whose GEMM 2 adds gate * row into the token-order y (zeroed
+// first) instead of writing y_sorted: the combine in GEMM 2's epilogue.
+int launch_grouped_ffn_combine(const moe_cfg& c, const void* x_sorted, const void* x,
+                               const int32_t* counts, const int32_t* offsets, const void* W13,
+                               const void* W2, void* h, const int32_t* order, const float* gate,
+                               void* y, void* ws, cudaStream_t st);
+
 int launch_grouped_ffn_pair(const moe_cfg& c, const void* x_sorted, const void* x,
                             const int32_t* counts, const int32_t* offsets, const void* W13,
                             const void* W2, void* h, void* y_sorted, int* status,

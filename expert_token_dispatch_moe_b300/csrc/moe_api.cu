@@ -257,6 +257,24 @@ MOE_API int moe_grouped_ffn(const moe_cfg* c, const moe_bf16* x_sorted, const mo
                             static_cast<cudaStream_t>(stream));
 }
 
+MOE_API int moe_grouped_ffn_combine(const moe_cfg* c, const moe_bf16* x_sorted, const moe_bf16* x,
+                                    const int32_t* counts, const int32_t* offsets,
+                                    const moe_bf16* W13, const moe_bf16* W2, moe_bf16* h,
+                                    const int32_t* order, const float* topk_gate, moe_bf16* y,
+                                    void* ws, size_t ws_bytes, void* stream) {
+  reset_launches();
+  MOE_TRY(moe_validate_cfg(c));
+  if (c->f < 128 || c->f % 128) return MOE_E_SHAPE;
+  if (c->E + c->has_shared > 1025) return MOE_E_SHAPE;
+  MOE_TRY(check_ptrs({x_sorted, counts, offsets, W13, W2, h, order, topk_gate, y}));
+  if (c->has_shared) MOE_TRY(check_ptrs({x}));
+  else MOE_TRY(check_opt({x}));
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  MOE_TRY(device_ok());
+  return launch_grouped_ffn_combine(*c, x_sorted, x, counts, offsets, W13, W2, h, order, topk_gate,
+                                    y, ws, static_cast<cudaStream_t>(stream));
+}
+
 MOE_API int moe_grouped_ffn_gather(const moe_cfg* c, const moe_bf16* x, const int32_t* order,
                                    const int32_t* counts, const int32_t* offsets,
                                    const moe_bf16* W13, const moe_bf16* W2, moe_bf16* h,

@@ -16,7 +16,7 @@ import torch
 
 from . import (MoeCfg, MoeLayerBufs, moe_backward_workspace_bytes, moe_combine, moe_combine_backward,
                moe_ep_layout, moe_grouped_ffn, moe_grouped_ffn_backward, moe_grouped_ffn_gather,
-               moe_grouped_ffn_train, moe_layer_forward, moe_layer_forward_host,
+               moe_grouped_ffn_train, moe_grouped_ffn_combine, moe_layer_forward, moe_layer_forward_host,
                moe_grouped_rows, moe_last_launch_count, moe_pack_backward, moe_pack_router,
                moe_pack_w13, moe_permute, moe_permute_backward, moe_route, moe_router_logits,
                moe_workspace_bytes, moe_workspace_init)
@@ -29,13 +29,21 @@ TC_ROUTER_MIN_E = 17
 
 class MoELayer:
     def __init__(self, cfg, W1, W3, W2, W_r=None, logit_bias=None, selection_bias=None,
-                 device=None, with_send_buf=True, tc_router=None, gather=False, train=False):
+                 device=None, with_send_buf=True, tc_router=None, gather=False, train=False,
+                 combine_in_epilogue=False):
         """gather=True: the permute computes indices only and GEMM 1 gathers its
         rows from x (moe_grouped_ffn_gather); x_sorted is not written.
         train=True: the forward keeps GEMM 1's pre-activations (self.g1) so the
-        backward need not recompute them."""
+        backward need not recompute them.
+        combine_in_epilogue=True: GEMM 2 adds its gated rows into y itself
+        (moe_grouped_ffn_combine) and y_sorted is not written; faster on the
+        large layers, but with more than two contributions per token the output
+        is not bit-reproducible from run to run."""
         self.cfg = cfg if isinstance(cfg, MoeCfg) else MoeCfg.from_layer(cfg)
         c = self.cfg
+        if combine_in_epilogue and (gather or train):
+            raise ValueError("combine_in_epilogue takes neither gather nor train")
+        self.combine_in_epilogue = combine_in_epilogue
         dev = torch.device(device or "cuda")
         self.device = dev
         i32, f32, bf16 = torch.int32, torch.float32, torch.bfloat16
@@ -125,6 +133,15 @@ class MoELayer:
             moe_grouped_ffn_train(c, self.x_sorted, x if c.has_shared else None, self.counts,
                                   self.offsets, self.W13, self.W2, self.h, self.y_sorted, self.g1,
                                   self.ws)
+        elif self.combine_in_epilogue:
+            out = self.y if y is None else y
+            moe_grouped_ffn_combine(c, self.x_sorted, x if c.has_shared else None, self.counts,
+                                    self.offsets, self.W13, self.W2, self.h, self.order,
+                                    self.topk_gate, out, self.ws)
+            pop()
+            n += moe_last_launch_count()
+            self.launches_per_forward = n
+            return out
         else:
             moe_grouped_ffn(c, self.x_sorted, x if c.has_shared else None, self.counts,
                             self.offsets, self.W13, self.W2, self.h, self.y_sorted, self.ws)
@@ -161,6 +178,8 @@ class MoELayer:
         (packed like W13), self.dW2 and self.dgate."""
         if self.gather:
             raise RuntimeError("backward needs the forward's x_sorted (gather=False)")
+        if self.combine_in_epilogue:
+            raise RuntimeError("backward needs the forward's y_sorted (combine_in_epilogue=False)")
         c = self.cfg
         if self.W13t is None:
             self._backward_buffers()

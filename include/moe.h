@@ -282,6 +282,26 @@ int moe_grouped_ffn(const moe_cfg* cfg, const moe_bf16* x_sorted, const moe_bf16
                     const moe_bf16* W13, const moe_bf16* W2, moe_bf16* h,
                     moe_bf16* y_sorted, void* ws, size_t ws_bytes, void* stream);
 
+/* moe_grouped_ffn with the combine (step 7) in GEMM 2's epilogue ("Token
+ * permutation and grouped GEMMs": production kernels fuse the permutation into
+ * the GEMM's loads and the combine into its epilogue).  GEMM 1 is that of
+ * moe_grouped_ffn; GEMM 2 does not write y_sorted: each routed row of
+ * assignment a adds bf16(topk_gate[a] * row) into y[a / k], each shared-expert
+ * row t adds its row into y[t], by 16-byte bf16 reductions in L2.
+ *   order      int32 [R]: the grouped rows' assignments (moe_permute's order)
+ *   topk_gate  fp32 [T, k]
+ *   y          bf16 [T, d] out: zeroed by the call, then accumulated
+ * Every add rounds to bf16, and the adds of one token arrive in no fixed order:
+ * with more than two contributions per token (k > 2, or k = 2 with a shared
+ * expert) y is not bit-reproducible from run to run; it stays within the
+ * layer's tolerance.  Runs on one-SM tiles whatever the layer's shape.  Other
+ * arguments and errors as for moe_grouped_ffn. */
+int moe_grouped_ffn_combine(const moe_cfg* cfg, const moe_bf16* x_sorted, const moe_bf16* x,
+                            const int32_t* counts, const int32_t* offsets,
+                            const moe_bf16* W13, const moe_bf16* W2, moe_bf16* h,
+                            const int32_t* order, const float* topk_gate, moe_bf16* y,
+                            void* ws, size_t ws_bytes, void* stream);
+
 /* The tiles moe_grouped_ffn takes for this configuration now (the rule above,
  * MOE_FFN_TILES read at this call): 1 for SM pairs (grouped_pair_kernel), 0 for
  * one-SM tiles (grouped_gemm_kernel), or a negative error code for an invalid
