@@ -105,7 +105,20 @@ def test_full_size_every_tile_against_oracle(m, name):
                                        [0, cfg.T - 1]]))
     y_ref, _ = oracle.moe_forward(x_np, s_np, cfg, StreamedExperts(W1), StreamedExperts(W3),
                                   StreamedExperts(W2), tokens=tokens)
-    assert_y_close(npf(layer.y[torch.from_numpy(tokens).to(dev)]), y_ref[tokens])
+    tok = torch.from_numpy(tokens).to(dev)
+    assert_y_close(npf(layer.y[tok]), y_ref[tokens])
+
+    # the combine in GEMM 2's epilogue at full size: the same sampled tokens
+    # against the oracle, and every token against the default path
+    y_f = torch.empty_like(layer.y)
+    m.moe_grouped_ffn_combine(layer.cfg, layer.x_sorted, x if cfg.has_shared else None,
+                              layer.counts, layer.offsets, layer.W13, layer.W2, layer.h,
+                              layer.order, layer.topk_gate, y_f, layer.ws)
+    torch.cuda.synchronize()
+    assert m.moe_get_device_status(layer.ws) == 0
+    assert_y_close(npf(y_f[tok]), y_ref[tokens])
+    err = (y_f.float() - layer.y.float()).abs().max().item()
+    assert err <= 2e-2 * layer.y.float().abs().max().item()
 
 
 @pytest.mark.parametrize("name,tc", [("mixtral", False), ("mixtral", True), ("dsv3", False),
