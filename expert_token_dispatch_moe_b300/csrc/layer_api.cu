@@ -29,9 +29,15 @@ MOE_API int moe_layer_forward(const moe_cfg* c, const moe_layer* L, const moe_bf
   MOE_STEP(moe_ep_layout(c, L->topk_idx, L->offsets, L->inv, L->count_mat, L->send_off,
                          L->recv_off, L->send_idx, L->send_buf ? x : nullptr, L->send_buf, L->ws,
                          L->ws_bytes, stream));
-  MOE_STEP(moe_grouped_ffn(c, L->x_sorted, c->has_shared ? x : nullptr, L->counts, L->offsets,
-                           L->W13, L->W2, L->h, L->y_sorted, L->ws, L->ws_bytes, stream));
-  MOE_STEP(moe_combine(c, L->y_sorted, L->inv, L->topk_gate, y, stream));
+  if (L->combine_in_epilogue) {
+    MOE_STEP(moe_grouped_ffn_combine(c, L->x_sorted, c->has_shared ? x : nullptr, L->counts,
+                                     L->offsets, L->W13, L->W2, L->h, L->order, L->topk_gate, y,
+                                     L->ws, L->ws_bytes, stream));
+  } else {
+    MOE_STEP(moe_grouped_ffn(c, L->x_sorted, c->has_shared ? x : nullptr, L->counts, L->offsets,
+                             L->W13, L->W2, L->h, L->y_sorted, L->ws, L->ws_bytes, stream));
+    MOE_STEP(moe_combine(c, L->y_sorted, L->inv, L->topk_gate, y, stream));
+  }
   reset_launches();
   note_launches(total);
   return MOE_OK;

@@ -211,7 +211,8 @@ class MoELayer:
                 counts=self.counts, offsets=self.offsets, order=self.order, inv=self.inv,
                 x_sorted=self.x_sorted, count_mat=self.count_mat, send_off=self.send_off,
                 recv_off=self.recv_off, send_idx=self.send_idx, send_buf=self.send_buf,
-                h=self.h, y_sorted=self.y_sorted, ws=self.ws)
+                h=self.h, y_sorted=self.y_sorted, ws=self.ws,
+                combine_in_epilogue=self.combine_in_epilogue)
         return self._c_bufs
 
     def forward_c(self, x, y=None):

@@ -90,3 +90,23 @@ def test_layer_option_uses_the_epilogue(m):
     assert_y_close(npf(y), npf(y_ref))
     with pytest.raises(RuntimeError):
         fused.backward(x, torch.zeros_like(y))
+
+
+@pytest.mark.parametrize("name", ["tiny", "ds_small"])
+def test_whole_forward_from_c_takes_the_flag(m, name):
+    """moe_layer_forward with combine_in_epilogue set: the same steps from C.
+    With two contributions per token (tiny) the bytes equal the Python-issued
+    forward's; otherwise the outputs agree within the layer's tolerance."""
+    cfg = CASES[name]
+    x = synth.make_x(cfg, device="cuda")
+    W1, W3, W2 = synth.make_expert_weights(cfg, device="cuda")
+    W_r, lbias = synth.make_router(cfg, device="cuda")
+    layer = m.MoELayer(cfg, W1, W3, W2, W_r=W_r, logit_bias=lbias, combine_in_epilogue=True)
+    y_py = layer.forward(x).clone()
+    y_c = layer.forward_c(x, torch.empty_like(y_py))
+    torch.cuda.synchronize()
+    assert m.moe_get_device_status(layer.ws) == 0
+    if cfg.k == 2 and not cfg.has_shared:
+        assert torch.equal(y_c.view(torch.int16), y_py.view(torch.int16))
+    else:
+        assert_y_close(npf(y_c), npf(y_py))
