@@ -158,7 +158,12 @@ int moe_route(const moe_cfg* cfg, const float* scores, const float* bias,
  *             row moves (for moe_grouped_ffn_gather, which reads rows from x).
  *   ws        workspace; keeps the per-(source rank, expert) histogram that
  *             moe_ep_layout reads
- * Capacity: expert e keeps its first `capacity` assignments in increasing a. */
+ * Capacity: expert e keeps its first `capacity` assignments in increasing a.
+ * Layers with up to 256 experts and more than 4096 assignments run as one
+ * cooperative launch whose grid barrier keeps its state in the workspace
+ * header (moe_workspace_init once; calls on one workspace must not overlap on
+ * the GPU).  A barrier wait that exceeds one second records
+ * MOE_E_DEVICE_TIMEOUT; the outputs are then unreliable. */
 int moe_permute(const moe_cfg* cfg, const moe_bf16* x, const int32_t* topk_idx,
                 int32_t* counts, int32_t* offsets, int32_t* order, int32_t* inv,
                 moe_bf16* x_sorted, void* ws, size_t ws_bytes, void* stream);
