@@ -19,5 +19,11 @@ k = E softmax = dense softmax), a dense-mask brute force of the whole layer and
 the pages' byte model.  The pages' capacity-padding percentages (7 %, 0.5 %,
 under 3 %) are not reproduced: their workload is not printed (parity unpinned
 for those figures; no function here claims them).
+
+A second statement of the forward path, one token at a time in plain C (fp64,
+counting sorts, per-token expert loops), lives in moe_loop.c and is reached
+through oracle.loop; it is pinned by tests/test_oracle_loop.py (the hand
+dispatch, brute-force routing, closed forms, planted mistakes) and agrees with
+the numpy statement to 1e-12.
 """
 from .moe_ref import *  # noqa: F401,F403
