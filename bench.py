@@ -763,9 +763,11 @@ class OracleSample:
                 f"estimated as (batch time with the FFN scaled by rows) x {self.cfg.T}/{self.n}")
 
 
-def cpu_baseline(cfg, x, W_r, lbias, layer, reps=3):
+def cpu_baseline(cfg, x, W_r, lbias, layer, reps=3, min_s=10.0, max_reps=40):
     """The oracle, as it stands, on the bounded sample of OracleSample (the
-    same procedure as --impl reference), median of `reps` runs."""
+    same procedure as --impl reference): after one warm run, at least `reps`
+    runs and more until about `min_s` seconds of host work (at most `max_reps`
+    runs); the median of the runs."""
     def weights(ids):
         W13, W2 = layer.W13, layer.W2
         n, f2, d = W13.shape
@@ -774,12 +776,16 @@ def cpu_baseline(cfg, x, W_r, lbias, layer, reps=3):
                 blk[:, :, 1].reshape(len(ids), f2 // 2, d), W2[ids])
     samp = OracleSample(cfg, x, W_r, lbias, weights)
     samp.run()  # warm
-    runs = [samp.run() for _ in range(reps)]
+    runs, spent = [], 0.0
+    while len(runs) < reps or (spent < min_s and len(runs) < max_reps):
+        runs.append(samp.run())
+        spent += runs[-1][0]
     meas = statistics.median(r[0] for r in runs)
     est = statistics.median(r[1] for r in runs)
     return {"value": cfg.T / est, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
             "sample": samp.describe(runs[0][2], runs[0][3]), "sample_s": meas,
-            "sample_tokens": samp.n, "estimated_step_s": est}
+            "sample_tokens": samp.n, "estimated_step_s": est, "sample_runs": len(runs),
+            "host_s": spent}
 
 
 def run_reference(args, cfg):

@@ -68,3 +68,30 @@ def test_tensor_peak_rule():
     assert b._tensor_peak(pk, {"power_cap_share": 0.2, "sm_mhz": 1500.0,
                                "sm_max_mhz": 2032.0}, 2.5)[0] == 1749.0
     assert b._tensor_peak(pk, None, 5.0)[0] == 1749.0
+
+
+def test_cpu_baseline_runs_bounded_samples():
+    """bench.py's cpu_baseline leg on the host: the oracle's sample repeated
+    until the requested seconds of host work (bounded by a run count), its
+    median reported with the runs and seconds it took."""
+    import importlib.util
+    import torch
+    sys.path.insert(0, ROOT)
+    import synth
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    cfg = synth.CONFIGS["tiny"].with_(T=256)
+    x = synth.make_x(cfg)
+    W_r, lbias = synth.make_router(cfg)
+    W1, W3, W2 = synth.make_expert_weights(cfg)
+
+    import types
+    # the layer's packed weights: W13 rows interleaved in 128-row blocks
+    W13 = torch.stack([torch.cat([torch.cat([W1[e, i:i + 128], W3[e, i:i + 128]])
+                                  for i in range(0, cfg.f, 128)]) for e in range(cfg.E)])
+    packed = types.SimpleNamespace(W13=W13, W2=W2)
+    got = b.cpu_baseline(cfg, x, W_r, lbias, packed, reps=2, min_s=0.2, max_reps=6)
+    assert 2 <= got["sample_runs"] <= 6 and got["host_s"] > 0
+    assert got["kind"] == "oracle" and got["value"] > 0 and got["unit"] == "tokens/s"
+    assert got["sample_runs"] == 6 or got["host_s"] >= 0.2
