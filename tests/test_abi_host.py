@@ -1,14 +1,21 @@
 """Host-side checks of the C ABI: the library loads, exports every entry point
 include/moe.h declares, and rejects bad arguments on the host before touching
-the device.  No kernel is launched (CPU only)."""
+the device.  No kernel is launched: the calls with fake device addresses that
+pass every host check (and would launch on a GPU) are made only where no CUDA
+device is visible, where they must fail with MOE_E_DEVICE."""
 import ctypes
 import os
 import re
 import subprocess
 
 import pytest
+import torch
 
 import synth
+
+# a call whose arguments pass the host checks reaches the device: with fake
+# addresses that may only happen on a machine without a GPU
+NO_GPU = not torch.cuda.is_available()
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -84,7 +91,8 @@ def test_host_argument_errors(m):
     assert lib.moe_permute(cfg, P, P, P, P, P, P, P, None, ws_need, None) == -4
     assert lib.moe_permute(cfg, P, P, P, P, P, P, P, P, ws_need - 1, None) == -4
     assert lib.moe_ep_layout(cfg, P, P, P, P, P, P, P, P, None, P, ws_need, None) == -1
-    assert lib.moe_grouped_ffn(cfg, P, None, P, P, P, P, P, P, P, ws_need, None) in (-6,)
+    if NO_GPU:
+        assert lib.moe_grouped_ffn(cfg, P, None, P, P, P, P, P, P, P, ws_need, None) == -6
     shared = m.MoeCfg.from_layer(synth.CONFIGS["tiny"].with_(has_shared=1))
     assert lib.moe_grouped_ffn(ctypes.byref(shared), P, None, P, P, P, P, P, P, P,
                                m.moe_workspace_bytes(shared), None) == -1
@@ -94,8 +102,7 @@ def test_host_argument_errors(m):
     assert lib.moe_pack_w13(ctypes.byref(odd_f), P, P, P, None) == -2
     bad = m.MoeCfg.from_layer(synth.CONFIGS["tiny"].with_(E=7))
     assert lib.moe_route(ctypes.byref(bad), P, None, P, P, None) == -2
-    import torch
-    if not torch.cuda.is_available():
+    if NO_GPU:
         assert lib.moe_route(cfg, P, None, P, P, None) == -6
         assert lib.moe_combine(cfg, P, P, P, P, None) == -6
     assert lib.moe_get_device_status(None, None) == -4
@@ -103,7 +110,7 @@ def test_host_argument_errors(m):
     assert lib.moe_selftest_wait_timeout(P + 4, 10 ** 6, None) == -3
     assert lib.moe_selftest_wait_timeout(P, 999, None) == -2
     assert lib.moe_selftest_wait_timeout(P, 10 ** 9 + 1, None) == -2
-    if not torch.cuda.is_available():
+    if NO_GPU:
         assert lib.moe_selftest_wait_timeout(P, 10 ** 6, None) == -6
     for code in range(-8, 1):
         assert lib.moe_strerror(code)
@@ -112,16 +119,19 @@ def test_host_argument_errors(m):
 def test_layer_entry_points_host_errors(m):
     """moe_layer_forward and moe_layer_forward_host check their arguments on the
     host; without an sm_103 GPU a valid call fails with MOE_E_DEVICE."""
-    import torch
     lib = m._lib
     c = m.MoeCfg.from_layer(synth.CONFIGS["tiny"])
     cfg = ctypes.byref(c)
     P = 1 << 20
     bufs = m.MoeLayerBufs()
-    for name, _ in m.MoeLayerBufs._fields_[:-1]:
+    for name, _ in m.MoeLayerBufs._fields_[:-3]:     # the device pointers
         setattr(bufs, name, P)
     bufs.ws_bytes = m.moe_workspace_bytes(c)
     lb = ctypes.byref(bufs)
+    # the gathered form and the combine epilogue do not go together
+    bufs.gather, bufs.combine_in_epilogue = 1, 1
+    assert lib.moe_layer_forward(cfg, lb, P, P, None) == -2
+    bufs.gather, bufs.combine_in_epilogue = 0, 0
     arr = (ctypes.c_void_p * 2)(P, P)
     assert lib.moe_layer_forward(cfg, None, P, P, None) == -1
     assert lib.moe_layer_forward_host(cfg, None, 1, arr, arr, arr, arr, None, None, None) == -1
@@ -135,7 +145,7 @@ def test_layer_entry_points_host_errors(m):
     bad = m.MoeCfg.from_layer(synth.CONFIGS["tiny"].with_(E=7))
     assert lib.moe_layer_forward_host(ctypes.byref(bad), lb, 1, arr, arr, arr, arr, None, None,
                                       None) == -2
-    if not torch.cuda.is_available():
+    if NO_GPU:
         assert lib.moe_layer_forward(cfg, lb, P, P, None) == -6
         assert lib.moe_layer_forward_host(cfg, lb, 1, arr, arr, arr, arr, None, None, None) == -6
 
