@@ -80,16 +80,18 @@ class MoeLayerBufs(ctypes.Structure):
                 ("W_r", "W_r_split", "logit_bias", "selection_bias", "W13", "W2", "scores",
                  "topk_idx", "topk_gate", "counts", "offsets", "order", "inv", "x_sorted",
                  "count_mat", "send_off", "recv_off", "send_idx", "send_buf", "h", "y_sorted",
-                 "ws")] + [("ws_bytes", ctypes.c_size_t), ("combine_in_epilogue", ctypes.c_int32)]
+                 "ws")] + [("ws_bytes", ctypes.c_size_t), ("combine_in_epilogue", ctypes.c_int32),
+                           ("gather", ctypes.c_int32)]
 
     @classmethod
-    def of(cls, combine_in_epilogue=False, **tensors) -> "MoeLayerBufs":
+    def of(cls, combine_in_epilogue=False, gather=False, **tensors) -> "MoeLayerBufs":
         b = cls()
-        for name, _ in cls._fields_[:-2]:
+        for name, _ in cls._fields_[:-3]:
             setattr(b, name, _ptr(tensors.get(name)))
         ws = tensors.get("ws")
         b.ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
         b.combine_in_epilogue = 1 if combine_in_epilogue else 0
+        b.gather = 1 if gather else 0
         return b
 
 

@@ -19,13 +19,15 @@ using namespace moe;
 MOE_API int moe_layer_forward(const moe_cfg* c, const moe_layer* L, const moe_bf16* x,
                               moe_bf16* y, void* stream) {
   if (!c || !L) return MOE_E_NULL;
+  if (L->gather && L->combine_in_epilogue) return MOE_E_SHAPE;
   int total = 0;
   if (L->W_r || L->W_r_split)
     MOE_STEP(moe_router_logits(c, x, L->W_r_split ? nullptr : L->W_r, L->W_r_split,
                                L->logit_bias, L->scores, L->ws, L->ws_bytes, stream));
   MOE_STEP(moe_route(c, L->scores, L->selection_bias, L->topk_idx, L->topk_gate, stream));
-  MOE_STEP(moe_permute(c, x, L->topk_idx, L->counts, L->offsets, L->order, L->inv, L->x_sorted,
-                       L->ws, L->ws_bytes, stream));
+  // the gathered form moves no rows here: GEMM 1 reads them from x
+  MOE_STEP(moe_permute(c, L->gather ? nullptr : x, L->topk_idx, L->counts, L->offsets, L->order,
+                       L->inv, L->gather ? nullptr : L->x_sorted, L->ws, L->ws_bytes, stream));
   MOE_STEP(moe_ep_layout(c, L->topk_idx, L->offsets, L->inv, L->count_mat, L->send_off,
                          L->recv_off, L->send_idx, L->send_buf ? x : nullptr, L->send_buf, L->ws,
                          L->ws_bytes, stream));
@@ -34,8 +36,13 @@ MOE_API int moe_layer_forward(const moe_cfg* c, const moe_layer* L, const moe_bf
                                      L->offsets, L->W13, L->W2, L->h, L->order, L->topk_gate, y,
                                      L->ws, L->ws_bytes, stream));
   } else {
-    MOE_STEP(moe_grouped_ffn(c, L->x_sorted, c->has_shared ? x : nullptr, L->counts, L->offsets,
-                             L->W13, L->W2, L->h, L->y_sorted, L->ws, L->ws_bytes, stream));
+    if (L->gather)
+      MOE_STEP(moe_grouped_ffn_gather(c, x, L->order, L->counts, L->offsets, L->W13, L->W2, L->h,
+                                      L->y_sorted, L->ws, L->ws_bytes, stream));
+    else
+      MOE_STEP(moe_grouped_ffn(c, L->x_sorted, c->has_shared ? x : nullptr, L->counts,
+                               L->offsets, L->W13, L->W2, L->h, L->y_sorted, L->ws, L->ws_bytes,
+                               stream));
     MOE_STEP(moe_combine(c, L->y_sorted, L->inv, L->topk_gate, y, stream));
   }
   reset_launches();

@@ -212,14 +212,14 @@ class MoELayer:
                 x_sorted=self.x_sorted, count_mat=self.count_mat, send_off=self.send_off,
                 recv_off=self.recv_off, send_idx=self.send_idx, send_buf=self.send_buf,
                 h=self.h, y_sorted=self.y_sorted, ws=self.ws,
-                combine_in_epilogue=self.combine_in_epilogue)
+                combine_in_epilogue=self.combine_in_epilogue, gather=self.gather)
         return self._c_bufs
 
     def forward_c(self, x, y=None):
         """The forward through the library's single entry point
         moe_layer_forward (same steps as forward, issued from C)."""
-        if self.gather or self.train:
-            raise RuntimeError("moe_layer_forward runs the rows path's inference forward")
+        if self.train:
+            raise RuntimeError("moe_layer_forward runs the inference forward")
         out = self.y if y is None else y
         moe_layer_forward(self.cfg, self.c_bufs(), x, out)
         self.launches_per_forward = moe_last_launch_count()
@@ -231,8 +231,8 @@ class MoELayer:
         its own stream, double-buffered on the device, the forward issued
         from C.  Returns once enqueued; synchronise the current stream to wait
         for the last result."""
-        if self.gather or self.train:
-            raise RuntimeError("moe_layer_forward_host runs the rows path's inference forward")
+        if self.train:
+            raise RuntimeError("moe_layer_forward_host runs the inference forward")
         s_in, s_out = self._copy_streams()
         self._stream_buffers()
         moe_layer_forward_host(self.cfg, self.c_bufs(), x_hosts, y_hosts, self._xbuf,

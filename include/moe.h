@@ -372,13 +372,18 @@ typedef struct moe_layer {
   size_t ws_bytes;
   int32_t combine_in_epilogue;   /* 1: moe_grouped_ffn_combine replaces moe_grouped_ffn +
                                     moe_combine (y_sorted unused; see its notes) */
+  int32_t gather;                /* 1: moe_permute computes the indices only and
+                                    moe_grouped_ffn_gather reads GEMM 1's rows from x
+                                    (x_sorted unused); not with combine_in_epilogue */
 } moe_layer;
 
 /* The forward on device tokens x (bf16 [T, d]) into y (bf16 [T, d]):
  * moe_router_logits (when L has router weights) -> moe_route -> moe_permute ->
  * moe_ep_layout -> moe_grouped_ffn -> moe_combine (or, with
- * L->combine_in_epilogue, moe_grouped_ffn_combine for the last two), on
- * `stream`.  Returns the first error of a step (nothing after it is launched). */
+ * L->combine_in_epilogue, moe_grouped_ffn_combine for the last two; with
+ * L->gather, moe_permute without the row move and moe_grouped_ffn_gather in
+ * place of moe_grouped_ffn), on `stream`.  Both flags set is MOE_E_SHAPE.
+ * Returns the first error of a step (nothing after it is launched). */
 int moe_layer_forward(const moe_cfg* cfg, const moe_layer* L, const moe_bf16* x, moe_bf16* y,
                       void* stream);
 

@@ -84,3 +84,28 @@ def test_gather_matches_unfused_full_size(m, name):
     assert torch.equal(a.h[rows].view(torch.int16), b.h[rows].view(torch.int16))
     assert torch.equal(a.y_sorted[rows].view(torch.int16), b.y_sorted[rows].view(torch.int16))
     assert torch.equal(a.y.view(torch.int16), b.y.view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["tiny", "ds_small", "skew_small"])
+def test_gather_whole_forward_from_c(m, name):
+    """moe_layer_forward and moe_layer_forward_host with the gather flag: the
+    same steps issued from C (the permute without its row move, GEMM 1 reading
+    rows from x) give the bytes of the Python-issued gathered forward, and of
+    the rows path."""
+    cfg = SMALL[name]
+    dev = torch.device("cuda")
+    x = synth.make_x(cfg, device=dev)
+    W1, W3, W2 = synth.make_expert_weights(cfg, device=dev)
+    W_r, lbias = synth.make_router(cfg, device=dev)
+    rows = m.MoELayer(cfg, W1, W3, W2, W_r=W_r, logit_bias=lbias, device=dev)
+    fused = m.MoELayer(cfg, W1, W3, W2, W_r=W_r, logit_bias=lbias, device=dev, gather=True)
+    y_rows = rows.forward(x).clone()
+    y_py = fused.forward(x).clone()
+    y_c = fused.forward_c(x, torch.empty_like(y_py))
+    x_host = x.cpu().pin_memory()
+    y_hosts = [torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+    fused.forward_host_c([x_host] * 3, y_hosts)
+    torch.cuda.synchronize()
+    assert m.moe_get_device_status(fused.ws) == 0
+    for y in [y_c, y_rows] + [h.to(dev) for h in y_hosts]:
+        assert torch.equal(y.view(torch.int16), y_py.view(torch.int16))
