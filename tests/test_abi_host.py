@@ -195,3 +195,26 @@ def test_ffn_tile_choice(m, monkeypatch):
     assert m.moe_ffn_pair_tiles(m.MoeCfg.from_layer(synth.CONFIGS["tiny"])) is True
     with pytest.raises(m.MoeError):
         m.moe_ffn_pair_tiles(m.MoeCfg.from_layer(synth.CONFIGS["tiny"].with_(k=0)))
+
+
+def test_noalloc_permute_host_errors(m):
+    """moe_permute_noalloc checks its arguments and its scratch limit on the
+    host, before it looks up its scratch array or launches anything: NULL and
+    misaligned pointers, one of x / x_sorted without the other, and a
+    configuration whose permute scratch exceeds the fixed 1 MiB."""
+    lib = m._lib
+    c = m.MoeCfg.from_layer(synth.CONFIGS["tiny"])
+    cfg = ctypes.byref(c)
+    P = 1 << 20
+    assert lib.moe_permute_noalloc(cfg, P, None, P, P, P, P, P, None) == -1
+    assert lib.moe_permute_noalloc(cfg, P, P + 4, P, P, P, P, P, None) == -3
+    assert lib.moe_permute_noalloc(cfg, P + 8, P, P, P, P, P, P, None) == -3
+    assert lib.moe_permute_noalloc(cfg, None, P, P, P, P, P, P, None) == -1
+    assert lib.moe_permute_noalloc(cfg, P, P, P, P, P, P, None, None) == -1
+    # per-(rank, expert) counts alone: 1024 ranks x 1024 experts x 4 B = 4 MiB
+    big = m.MoeCfg.from_layer(synth.CONFIGS["tiny"].with_(T=1024, E=1024, k=2, n_ep=1024, d=64))
+    assert lib.moe_permute_noalloc(ctypes.byref(big), P, P, P, P, P, P, P, None) == -9
+    bad = m.MoeCfg.from_layer(synth.CONFIGS["tiny"].with_(E=7))
+    assert lib.moe_permute_noalloc(ctypes.byref(bad), P, P, P, P, P, P, P, None) == -2
+    if NO_GPU:
+        assert lib.moe_permute_noalloc(cfg, P, P, P, P, P, P, P, None) == -6
