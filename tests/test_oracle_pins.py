@@ -520,3 +520,40 @@ def test_planted_wrong_expert_in_expert_rows_is_caught(monkeypatch):
         return real(X, W3, W1) if calls["n"] % 2 == 0 else real(X, W1, W3)
     monkeypatch.setattr(moe_ref, "swiglu_hidden", shifted)
     assert _fails(lambda: test_expert_rows_per_row_brute_force(dict(E=6, k=2)))
+
+
+def test_dsv3_worked_example_bytes_and_flops():
+    """The pages' worked example at DeepSeek-V3's shape ("Expert parallelism",
+    "A worked example at DeepSeek-V3's shape"): 693 MB cross the network per
+    GPU per layer (FP8 dispatch plus BF16 combine), and the experts' compute is
+    2.9e12 FLOPs.  The bytes are counted from the oracle's layout of a
+    uniformly routed batch of n_ep * T_loc tokens; the FLOPs from the benchmark's
+    model of 6*d*d_e per assignment."""
+    import importlib.util
+    g = _load("dsv3_worked_example.json")
+    d, k, T_loc, n_ep = g["d"], g["k"], g["T_loc"], g["n_ep"]
+    E = 256
+    T = T_loc * n_ep
+    rng = np.random.default_rng(12)
+    # balanced routing: each token's k distinct experts uniformly at random
+    idx = np.argsort(rng.random((T, E)), axis=1)[:, :k]
+    p = oracle.permute(idx, E)
+    C = oracle.ep_layout(idx, p["inv"], E, n_ep, T)["C"]
+    disp, comb = oracle.alltoall_bytes(C, d, g["s_dispatch"], g["s_combine"])
+    per_gpu = (disp + comb).mean()
+    closed = T_loc * k * d * (g["s_dispatch"] + g["s_combine"]) * (n_ep - 1) / n_ep
+    assert closed / 1e6 == pytest.approx(g["bytes_mb"], abs=0.7)
+    assert per_gpu == pytest.approx(closed, rel=2e-3)
+    assert closed / (g["ib_gbs"] * 1e9) * 1e3 == pytest.approx(g["ib_ms"], abs=0.05)
+    assert closed / (g["nvlink_gbs"] * 1e9) * 1e3 == pytest.approx(g["nvlink_ms"], abs=0.05)
+    spec = importlib.util.spec_from_file_location(
+        "bench_mod", os.path.join(os.path.dirname(GOLDEN), "..", "bench.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    cfg = synth.LayerConfig("worked", T=T_loc, d=d, E=E, k=k, f=g["d_e"], n_ep=1,
+                            score_fn="sigmoid", norm_topk=1)
+    counts = np.full(E, T_loc * k // E)
+    flops = b._algorithmic(cfg, counts)["ffn_flops"]
+    assert flops == 4096 * 8 * 6 * 7168 * 2048
+    assert flops == pytest.approx(g["flops"], rel=0.01)
+    assert flops / (g["peak_tflops"] * 1e12) * 1e3 == pytest.approx(g["compute_ms"], abs=0.05)
