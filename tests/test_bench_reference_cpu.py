@@ -95,3 +95,37 @@ def test_cpu_baseline_runs_bounded_samples():
     assert 2 <= got["sample_runs"] <= 6 and got["host_s"] > 0
     assert got["kind"] == "oracle" and got["value"] > 0 and got["unit"] == "tokens/s"
     assert got["sample_runs"] == 6 or got["host_s"] >= 0.2
+
+
+def test_serving_ridge_reasoning():
+    """The pages' serving ridge ("Expert parallelism", "Serving"): an expert's
+    product with n tokens does 2 n d d_e FLOPs per weight matrix and reads d d_e
+    2-byte weights, about n FLOPs per byte; an H100 needs 989/3.35 ~ 295 FLOPs
+    per byte, so about 300 tokens per expert, 300 E / k ~ 9,600 tokens for
+    DeepSeek-V3.  The benchmark's FLOP and weight-byte models give the same
+    intensity, and its roofline puts a layer on the tensor side exactly when the
+    rows per expert pass the ridge of the peaks it divides by."""
+    import importlib.util
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import synth
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    assert round(989 / 3.35) == 295
+    assert 300 * 256 // 8 == 9600
+    for n in (4, 64, 288, 1024):
+        cfg = synth.CONFIGS["dsv3"].with_(T=n * 256 // 8, has_shared=0)
+        counts = np.full(cfg.E, n)
+        flops = b._algorithmic(cfg, counts)["ffn_flops"]
+        weight_bytes = cfg.E * 3 * cfg.d * cfg.f * 2
+        assert flops / weight_bytes == n
+        # the model's bytes also hold the activations, so its ridge sits a little above n
+        ffn_bytes = b._ffn_bytes(cfg, counts)
+        assert ffn_bytes > weight_bytes
+        pk = {"hbm_gbs": 6503.1, "bf16_tflops": 1749.0, "bf16_tflops_sustained": 1350.5,
+              "source": "measured"}
+        line = b._roofline(cfg, 1.0, flops, ffn_bytes, pk, {}, 0.1)
+        ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)   # ~269 FLOPs per byte
+        assert line["bound"] == ("tensor" if flops / ffn_bytes >= ridge else "hbm")
+        assert line["bound"] == ("tensor" if n >= 1024 else "hbm")   # 288 rows: at the ridge, HBM side
