@@ -557,3 +557,18 @@ def test_dsv3_worked_example_bytes_and_flops():
     assert flops == 4096 * 8 * 6 * 7168 * 2048
     assert flops == pytest.approx(g["flops"], rel=0.01)
     assert flops / (g["peak_tflops"] * 1e12) * 1e3 == pytest.approx(g["compute_ms"], abs=0.05)
+
+
+def test_decode_batch_tokens_per_expert():
+    """"flops/sched-expert-parallelism", notes: with 256 experts and top-8 the
+    batch per expert is B*8/256 = B/32, so B = 128 gives each expert 4 tokens on
+    average.  The decode workload is that batch; the oracle's counts of a routed
+    decode batch average exactly 4 per expert (every token keeps k distinct
+    experts, dropless)."""
+    cfg = synth.CONFIGS["dsv3_decode"]
+    assert (cfg.T, cfg.E, cfg.k) == (128, 256, 8) and cfg.T * cfg.k / cfg.E == 4
+    s = synth.make_scores(cfg).numpy()
+    idx = oracle.select_experts(s, cfg.k, None, cfg.n_groups, cfg.topk_groups)
+    counts = oracle.permute(idx, cfg.E)["counts"]
+    assert counts.sum() == 128 * 8 and counts.mean() == 4.0
+    assert all(len(set(row)) == cfg.k for row in idx.tolist())
